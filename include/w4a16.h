@@ -1,0 +1,181 @@
+/*
+ * w4a16.h - C ABI of libw4a16.so: the W4A16 mixed-precision linear layer on one NVIDIA GB300 (sm_103a).
+ *
+ *     C[M, N] = A[M, K] . dequant(W) (+ bias[N])
+ *
+ * A is fp16 or bf16. W is stored as unsigned 4-bit values packed eight per int32 along N
+ * (b_q[K, N/8]) with one scale per (group of G rows of K, output column) and a zero point that
+ * is either the fixed bias zp_bias (8 for the symmetric uint4b8 type) or unpacked from
+ * qzeros[K/G, N/8]:   dequant(W)[k, n] = (q[k, n] - zp[k/G, n]) * scales[k/G, n].
+ *
+ * Sources (the pages describing the method):
+ *   - "PR #51453 report: register Triton W4A16 GEMM as custom op" - key source snippets: the facade
+ *     triton_w4a16_gemm(a, b_q, scales, qzeros, group_size, zp_bias=8), the fake implementation
+ *     (out shape (M, b_q.size(1)*8), dtype and device of a), and the fake-impl test shapes
+ *     a(4,256) b_q(256,64) scales(2,512) group_size 128 -> out(4,512).
+ *   - "PR #43731 report: TritonW4A16LinearKernel as CUDA fallback" - key source snippets:
+ *     can_implement() rejections (fp16/bf16 activations only, N % 8 == 0, no g_idx, supported group
+ *     sizes or G == K) and their reason strings; motivation: K or N = 2112 must work.
+ *   - "PR #40977 report: ROCm RDNA hybrid W4A16" - key source snippets: the test reference
+ *     (dequant in high precision, bias added before the cast to the activation dtype), and the
+ *     runtime routing on M between a skinny split-K decode kernel and a tiled prefill kernel.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensor pointers are device pointers owned by the caller, contiguous and row-major. Natural
+ *     alignment is required (2 bytes for 16-bit tensors, 4 bytes for int32). Higher alignment
+ *     (16 bytes) and N % 32 == 0, K % 16 == 0 unlock the fast paths; otherwise a generic GPU path runs.
+ *   - scales, bias, out and w_out have the dtype of A.
+ *   - Calls are stream-ordered on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *     w4a16_gemm, w4a16_pack, w4a16_unpack and w4a16_dequant allocate nothing, do not synchronise and
+ *     read nothing back to the host, and keep no pointer after they return.
+ *   - Errors are reported by the returned status; a human-readable reason for the last failure on the
+ *     calling thread is available from w4a16_last_error(). Validation happens before any launch, so a
+ *     rejected call touches no memory. The library never aborts the process and device code never traps.
+ *   - Rows M may be 0 (nothing is launched). There is no g_idx (activation reordering) argument: the
+ *     pages' kernel rejects it.
+ */
+#ifndef W4A16_H_
+#define W4A16_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *w4a16_stream_t;
+
+typedef enum { W4A16_F16 = 0, W4A16_BF16 = 1 } w4a16_dtype;
+
+typedef enum {
+  W4A16_OK = 0,
+  W4A16_ERR_INVALID_ARG = 1, /* shapes, null pointers, aliasing, zp_bias range            */
+  W4A16_ERR_UNSUPPORTED = 2, /* dtype or group size outside what the layer defines         */
+  W4A16_ERR_MISALIGNED = 3,  /* a pointer is not naturally aligned for its element type     */
+  W4A16_ERR_CUDA = 4,        /* a CUDA runtime call failed; the message carries its text     */
+  W4A16_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (see w4a16_get_device_error) */
+} w4a16_status;
+
+/* Kernel paths chosen by the runtime dispatcher (w4a16_plan / w4a16_debug_selected_path). */
+typedef enum {
+  W4A16_PATH_NONE = 0,    /* M == 0: nothing to do                                            */
+  W4A16_PATH_GENERIC = 1, /* any alignment: one thread per (8 output columns, 8 rows), K-sliced   */
+  W4A16_PATH_DECODE = 2,  /* M <= 64: split-K skinny GEMM, cp.async 16-byte streams, mma.sync,
+                             in-register magic-number dequant, cluster (DSMEM) split-K reduction */
+  W4A16_PATH_PREFILL = 3  /* large M: TMA-fed tcgen05/TMEM GEMM, int4 tiles dequantised into
+                             shared memory before each UMMA                                     */
+} w4a16_path;
+
+/* Launch plan for one w4a16_gemm call. Filled by w4a16_plan; informational. */
+typedef struct {
+  int32_t path;          /* w4a16_path                                                     */
+  int32_t words_per_lane;/* DECODE: packed words per lane per row (1, 2 or 4)                 */
+  int32_t m_tile;        /* rows of A per CTA                                              */
+  int32_t n_tile;        /* output columns per CTA                                         */
+  int32_t k_split;       /* CTAs (one cluster) sharing one output tile along K               */
+  int32_t warps;         /* warps per CTA                                                  */
+  int64_t grid;          /* CTAs launched                                                  */
+  int32_t smem_bytes;    /* dynamic shared memory per CTA                                  */
+  int32_t reserved;
+} w4a16_plan_t;
+
+/*
+ * w4a16_pack - pack 4-bit values eight per int32 along the last dimension.
+ *   q:      device, uint8 [rows, n], each value 0..15 (higher bits are ignored)
+ *   packed: device, int32 [rows, n/8]; nibble j (bits 4j..4j+3) of word c receives q[r, 8c+j].
+ * The nibble order inside a word is not printed on the pages; sequential little-endian order is
+ * the plain reading of "eight values packed along N" (PR #51453 report, implementation breakdown:
+ * N = b_q.shape[1] * 8). Used for weights [K, N] -> b_q and zero points [K/G, N] -> qzeros.
+ * Errors: INVALID_ARG if rows < 0, n <= 0, n % 8 != 0, a null pointer with rows > 0, or overlap.
+ */
+w4a16_status w4a16_pack(const uint8_t *q, int32_t *packed, int64_t rows, int64_t n,
+                        w4a16_stream_t stream);
+
+/* w4a16_unpack - inverse of w4a16_pack: packed int32 [rows, n/8] -> uint8 [rows, n] (values 0..15). */
+w4a16_status w4a16_unpack(const int32_t *packed, uint8_t *q, int64_t rows, int64_t n,
+                          w4a16_stream_t stream);
+
+/*
+ * w4a16_dequant - materialise dequant(W) in the activation dtype:
+ *   w_out[k, n] = RNE_dtype((q[k, n] - zp[k/G, n]) * scales[k/G, n])
+ * i.e. the exact product rounded once to nearest-even. These are exactly the values the GEMM
+ * kernels feed to their multiply-accumulate (dequantisation rule: PR #40977 report, key source
+ * snippets, test reference; zp = qzeros nibble, or zp_bias when qzeros is NULL).
+ *   b_q [k, n/8] int32, scales [k/G, n] dtype, qzeros [k/G, n/8] int32 or NULL, w_out [k, n] dtype.
+ * Errors: as w4a16_gemm's validation (dtype, n % 8, group size, k % G, zp_bias, nulls, overlap).
+ */
+w4a16_status w4a16_dequant(const int32_t *b_q, const void *scales, const int32_t *qzeros,
+                           int64_t k, int64_t n, int group_size, int zp_bias, w4a16_dtype dtype,
+                           void *w_out, w4a16_stream_t stream);
+
+/*
+ * w4a16_gemm - out[M, N] = cast_dtype( A[M, K] . dequant(W) (+ bias) ), fp32 accumulation.
+ *   a       [m, k]    dtype            activations (PR #51453 facade argument a)
+ *   b_q     [k, n/8]  int32            packed 4-bit weights
+ *   scales  [k/G, n]  dtype            per-group scales
+ *   qzeros  [k/G, n/8] int32 or NULL   packed zero points; NULL selects the fixed zp_bias
+ *   group_size G in {32, 64, 128} or G == k (per-channel); k % G == 0
+ *   zp_bias 0..15 (8 = symmetric uint4b8); ignored when qzeros is given
+ *   bias    [n] dtype or NULL          added in fp32 before the cast (PR #40977 test reference)
+ *   out     [m, n]    dtype            written; must not overlap any input
+ * The kernel and its tile, split-K factor and cluster size are chosen on every call from the runtime
+ * M, K, N, G and the device (SM count, shared memory), never frozen between calls - the failure the
+ * PR #51453 report describes (prefill tile configuration reused for decode under compilation).
+ * Dequantised weights are rounded to the dtype before the product, exactly as w4a16_dequant returns
+ * them; the sum is kept in fp32 and rounded once (nearest-even) after the bias.
+ * Errors: UNSUPPORTED (dtype, group size), INVALID_ARG (shapes, nulls, zp_bias, overlap),
+ *         MISALIGNED (natural alignment), CUDA (launch failure), TIMEOUT (a previous kernel of this
+ *         library gave up a bounded wait; reported once, then cleared).
+ */
+w4a16_status w4a16_gemm(const void *a, const int32_t *b_q, const void *scales, const int32_t *qzeros,
+                        int group_size, int zp_bias, const void *bias, void *out, int64_t m,
+                        int64_t k, int64_t n, w4a16_dtype dtype, w4a16_stream_t stream);
+
+/*
+ * w4a16_can_implement - host-only check of a layer configuration, mirroring
+ * TritonW4A16LinearKernel.can_implement (PR #43731 report, key source snippets): returns W4A16_OK or
+ * the rejection status, with the reason available from w4a16_last_error(). No device access.
+ *   dtype: W4A16_F16 / W4A16_BF16 (other values rejected); has_g_idx != 0 is rejected.
+ */
+w4a16_status w4a16_can_implement(int64_t k, int64_t n, int group_size, int dtype, int has_g_idx);
+
+/*
+ * w4a16_plan - host-only: the launch plan w4a16_gemm would use for these sizes on a device with
+ * `num_sms` SMs (num_sms <= 0: query the current device). Pointer alignment is assumed to be 16 bytes.
+ */
+w4a16_status w4a16_plan(int64_t m, int64_t k, int64_t n, int group_size, int dtype, int has_zp,
+                        int num_sms, w4a16_plan_t *plan);
+
+/* Thread-local, NUL-terminated reason for the last failing call on this thread ("" if none). */
+const char *w4a16_last_error(void);
+
+/*
+ * w4a16_get_device_error - reads and clears the device-side error word of the current device:
+ * W4A16_ERR_TIMEOUT if a kernel of this library gave up a bounded wait (it then wrote no result and
+ * released its resources), W4A16_OK otherwise. Synchronises the current device.
+ */
+w4a16_status w4a16_get_device_error(void);
+
+/* Path w4a16_gemm would choose for these sizes on the current device (a w4a16_path value), or -1. */
+int w4a16_debug_selected_path(int64_t m, int64_t k, int64_t n, int group_size);
+
+/*
+ * w4a16_debug_set_wait_limit_ns - sets the limit of every bounded device-side wait (nanoseconds;
+ * 0 restores the default of 2 s). A test sets a tiny limit to make a wait give up and checks that
+ * the TIMEOUT status is reported without hanging the GPU. Synchronous.
+ */
+w4a16_status w4a16_debug_set_wait_limit_ns(uint64_t ns);
+
+/* Number of kernels this library has launched in this process (all devices, all threads). */
+uint64_t w4a16_debug_launch_count(void);
+
+/* Library version string. */
+const char *w4a16_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H_ */

@@ -1,0 +1,86 @@
+"""Test helpers: move synthetic cases to the GPU, call the library, compare with the oracle."""
+from __future__ import annotations
+
+import contextlib
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from oracle import ieee
+
+TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def bits_to_torch(bits: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(TORCH_DT[dtype])
+    return t.to(device)
+
+
+def torch_to_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def case_tensors(c, device="cuda"):
+    d = {
+        "a": bits_to_torch(c.a, c.dtype, device),
+        "b_q": torch.from_numpy(c.b_q).to(device),
+        "scales": bits_to_torch(c.scales, c.dtype, device),
+        "qzeros": None if c.qzeros is None else torch.from_numpy(c.qzeros).to(device),
+        "bias": None if c.bias is None else bits_to_torch(c.bias, c.dtype, device),
+    }
+    return d
+
+
+@contextlib.contextmanager
+def forced_path(path):
+    old = os.environ.get("W4A16_FORCE_PATH")
+    if path is None:
+        os.environ.pop("W4A16_FORCE_PATH", None)
+    else:
+        os.environ["W4A16_FORCE_PATH"] = path
+    try:
+        yield
+    finally:
+        if old is None:
+            os.environ.pop("W4A16_FORCE_PATH", None)
+        else:
+            os.environ["W4A16_FORCE_PATH"] = old
+
+
+def sample_cols(N: int, rng: np.random.Generator, k: int = 384) -> np.ndarray:
+    """Columns to check on wide outputs: both edges, every n % 8 position, tile edges, random."""
+    base = set(range(0, min(N, 272))) | set(range(max(0, N - 272), N))
+    base |= set(rng.integers(0, N, size=k).tolist())
+    return np.array(sorted(base), dtype=np.int64)
+
+
+def check_against_oracle(c, out_bits: np.ndarray, rows=None, cols=None, label=""):
+    """Assert |out - ref| <= atol + rtol*|ref| against the dequant-T product, and the rigorous
+    bound against the exact-weight product. Returns a dict of error statistics."""
+    kw = dict(rows=rows, cols=cols)
+    sub = out_bits
+    if rows is not None:
+        sub = sub[np.asarray(rows)]
+    if cols is not None:
+        sub = sub[:, np.asarray(cols)]
+    ref_t = oracle.gemm_ref(c.a, c.b_q, c.scales, c.qzeros, c.G, c.zp_bias, c.bias, c.dtype,
+                            weights="dequant_t", **kw)
+    ok = oracle.within_tolerance(sub, ref_t, c.dtype)
+    out = ieee.t_decode(sub, c.dtype)
+    err = np.abs(out - ref_t)
+    atol, rtol = oracle.tolerance(c.dtype)
+    if not ok.all():
+        bad = np.argwhere(~ok)[:8]
+        details = [(int(i), int(j), float(out[i, j]), float(ref_t[i, j])) for i, j in bad]
+        raise AssertionError(f"{label}: {int((~ok).sum())} of {ok.size} outputs outside "
+                             f"{atol}+{rtol}|ref| (max err {err.max():.3g}); first: {details}")
+    ref_e = oracle.gemm_ref(c.a, c.b_q, c.scales, c.qzeros, c.G, c.zp_bias, c.bias, c.dtype,
+                            weights="exact", **kw)
+    bound = oracle.weight_rounding_bound(c.a, c.b_q, c.scales, c.qzeros, c.G, c.zp_bias, c.dtype, **kw)
+    ok_e = np.abs(out - ref_e) <= atol + rtol * np.abs(ref_t) + bound * (1 + 1e-9)
+    if not ok_e.all():
+        raise AssertionError(f"{label}: exact-weight bound violated at {int((~ok_e).sum())} outputs")
+    return {"max_err": float(err.max()) if err.size else 0.0,
+            "max_rel_tol_use": float((err / (atol + rtol * np.abs(ref_t))).max()) if err.size else 0.0}

@@ -1,0 +1,141 @@
+"""Host-side tests of the C ABI (no GPU): the library loads and exports every declared symbol,
+validation rejects what the pages' can_implement rejects (before touching any memory), and the
+runtime dispatcher picks paths and split-K factors from the runtime shape."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def w():
+    from w4a16_int4_weight_group_gb300 import build
+    build.build()
+    import w4a16_int4_weight_group_gb300 as mod
+    mod.lib()
+    return mod
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a16_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("w4a16_pack", "w4a16_gemm", "w4a16_unpack", "w4a16_dequant", "w4a16_can_implement",
+                 "w4a16_last_error", "w4a16_get_device_error", "w4a16_debug_selected_path"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(w):
+    names = declared_functions()
+    lib = w.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", w.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (w4a16_\w+)", out))
+    assert set(names) <= exported
+    assert {s[0] for s in w.SIGNATURES} == set(names)
+
+
+def test_can_implement_reasons_follow_the_pages(w):
+    assert w.w4a16_can_implement(2112, 1152, 32, 1) == (True, "")
+    assert w.w4a16_can_implement(256, 512, 128, 0) == (True, "")
+    ok, why = w.w4a16_can_implement(256, 516, 128, 0)
+    assert not ok and "must be divisible by 8" in why and "8 int4 values packed per int32" in why
+    ok, why = w.w4a16_can_implement(256, 512, 128, 7)
+    assert not ok and "float16/bfloat16" in why
+    ok, why = w.w4a16_can_implement(256, 512, 128, 0, has_g_idx=True)
+    assert not ok and "g_idx" in why
+    ok, why = w.w4a16_can_implement(256, 512, 96, 0)
+    assert not ok and "Group size 96 not supported" in why
+    # group_size == K (per-channel) is allowed for any K
+    assert w.w4a16_can_implement(100, 512, 100, 0) == (True, "")
+    for g in (32, 64):
+        assert w.w4a16_can_implement(2112, 4224, g, 1) == (True, "")
+    # 2112 = 16.5 * 128: groups of 128 do not tile K
+    ok, why = w.w4a16_can_implement(2112, 4224, 128, 1)
+    assert not ok and "multiple of group_size" in why
+
+
+def _gemm(w, a=0x1000, b_q=0x2000, scales=0x3000, qzeros=None, G=32, zp=8, bias=None, out=0x100000,
+          m=4, k=64, n=64, dt=0):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return w.lib().w4a16_gemm(p(a), p(b_q), p(scales), p(qzeros), G, zp, p(bias), p(out), m, k, n, dt, None)
+
+
+def test_gemm_validation_rejects_before_any_launch(w):
+    before = w.w4a16_debug_launch_count()
+    assert _gemm(w, dt=3) == 2 and "float16/bfloat16" in w.last_error()
+    assert _gemm(w, n=60) == 1 and "divisible by 8" in w.last_error()
+    assert _gemm(w, G=48) == 2
+    assert _gemm(w, k=96, G=64) == 1 and "multiple of group_size" in w.last_error()
+    assert _gemm(w, zp=16) == 1 and "zp_bias" in w.last_error()
+    assert _gemm(w, zp=-1) == 1
+    assert _gemm(w, a=None) == 1 and "NULL" in w.last_error()
+    assert _gemm(w, out=None) == 1
+    assert _gemm(w, m=-1) == 1
+    assert _gemm(w, k=0) == 1
+    assert _gemm(w, a=0x1001) == 3 and "aligned" in w.last_error()
+    assert _gemm(w, b_q=0x2002) == 3
+    # out overlapping an input
+    assert _gemm(w, out=0x2000) == 1 and "overlaps" in w.last_error()
+    assert _gemm(w, out=0x1000 + 4 * 64 * 2 - 2) == 1
+    # M == 0: nothing to do, no device access, OK
+    assert _gemm(w, m=0, a=None, out=None) == 0
+    assert w.w4a16_debug_launch_count() == before
+
+
+def test_pack_validation(w):
+    L = w.lib()
+    assert L.w4a16_pack(ctypes.c_void_p(0x1000), ctypes.c_void_p(0x8000), 4, 12, None) == 1
+    assert L.w4a16_pack(None, ctypes.c_void_p(0x8000), 4, 16, None) == 1
+    assert L.w4a16_pack(ctypes.c_void_p(0x1000), ctypes.c_void_p(0x8002), 4, 16, None) == 3
+    assert L.w4a16_pack(ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1010), 4, 16, None) == 1  # overlap
+    assert L.w4a16_pack(None, None, 0, 16, None) == 0
+
+
+def test_dispatcher_decode_for_small_m_and_split_k(w):
+    # decode workloads of the pages: M <= 8 takes the split-K decode path
+    for m in (1, 2, 4, 5, 8):
+        for k, n in ((1152, 4224), (2112, 1152), (2560, 19456), (9728, 2560)):
+            p = w.w4a16_plan(m, k, n, 32 if k in (1152, 2112) else 128, 0, False, 152)
+            assert p["path_name"] == "decode", (m, k, n, p)
+            assert p["m_tile"] == 8
+            assert 1 <= p["k_split"] <= 8
+            assert p["grid"] <= 2 * 152
+    # a narrow layer gets split along K across a cluster
+    p = w.w4a16_plan(1, 2112, 1152, 32, 1, False, 152)
+    assert p["k_split"] > 1
+    # a wide one does not need to
+    p = w.w4a16_plan(1, 2560, 19456, 128, 0, True, 152)
+    assert p["k_split"] == 1 and p["grid"] == 152
+
+
+def test_dispatcher_uses_runtime_m_not_a_frozen_config(w):
+    # the same layer, decode and prefill sizes, in any order: plans depend only on the runtime M
+    k, n, g = 5120, 7168, 128
+    seq = [1, 4096, 8, 1024, 1, 2, 8192, 5]
+    plans = [w.w4a16_plan(m, k, n, g, 1, True, 152) for m in seq]
+    again = [w.w4a16_plan(m, k, n, g, 1, True, 152) for m in seq[::-1]][::-1]
+    assert plans == again
+    assert plans[0]["m_tile"] < plans[1]["m_tile"] or plans[1]["path_name"] != "decode"
+
+
+def test_dispatcher_generic_for_unaligned_shapes(w):
+    # N % 32 != 0 or K % 16 != 0 cannot use the 16-byte streaming paths
+    assert w.w4a16_plan(4, 256, 520, 128, 0, False, 152)["path_name"] == "generic"
+    assert w.w4a16_plan(4, 100, 512, 100, 0, False, 152)["path_name"] == "generic"
+    assert w.w4a16_plan(0, 256, 512, 128, 0, False, 152)["path_name"] == "none"
+
+
+def test_plan_rejects_bad_config(w):
+    with pytest.raises(w.W4A16Error):
+        w.w4a16_plan(4, 256, 516, 128, 0, False, 152)

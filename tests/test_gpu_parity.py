@@ -1,0 +1,195 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle on the same seeded inputs.
+
+Bit-exact for pack / unpack / dequant and for the identity-A product (one non-zero product per
+output is exact in fp32, so the output equals the dequantised weight); within the layer's tolerance
+|out - ref| <= atol + rtol*|ref| (fp16 1e-2/1e-2, bf16 2e-2/2e-2) for the product, where ref is the
+fp64 product over the dequantised weights; plus the rigorous bound against exact-weight fp64.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests._util import (bits_to_torch, case_tensors, check_against_oracle, forced_path, sample_cols,
+                         torch_to_bits)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from w4a16_int4_weight_group_gb300 import build
+    build.build()
+    import w4a16_int4_weight_group_gb300 as mod
+    mod.lib()
+    return mod
+
+
+def run(w, c, path=None, out=None):
+    t = case_tensors(c)
+    with forced_path(path):
+        o = w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], c.G, c.zp_bias, t["bias"], out=out)
+    torch.cuda.synchronize()
+    return torch_to_bits(o)
+
+
+def supported_paths(w, c):
+    paths = ["generic"]
+    plan = w.w4a16_plan(c.M, c.K, c.N, c.G, 1 if c.dtype == "bf16" else 0, c.asym, 0)
+    for p in ("decode", "prefill"):
+        with forced_path(p):
+            if w.w4a16_plan(c.M, c.K, c.N, c.G, 1 if c.dtype == "bf16" else 0, c.asym, 0)["path_name"] == p:
+                paths.append(p)
+    return paths, plan["path_name"]
+
+
+# ------------------------------------------------------------------------------------------------
+# layout kernels: bit-exact
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("rows,n", [(1, 8), (37, 232), (1152, 4224), (3, 8 * 4099)])
+def test_pack_unpack_bitexact(w, rows, n):
+    q = synth.random_nibbles(rows, n, seed=rows + n)
+    packed = w.w4a16_pack(torch.from_numpy(q).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(packed.cpu().numpy(), oracle.pack(q))
+    back = w.w4a16_unpack(packed)
+    torch.cuda.synchronize()
+    assert np.array_equal(back.cpu().numpy(), q)
+
+
+@pytest.mark.parametrize("K,N,G,dtype,asym,zp", [
+    (256, 512, 128, "f16", False, 8), (2112, 1152, 32, "bf16", False, 8), (2560, 3840, 128, "f16", True, 8),
+    (100, 520, 100, "bf16", True, 8), (64, 8, 64, "f16", False, 0), (128, 64, 32, "bf16", False, 15)])
+def test_dequant_bitexact(w, K, N, G, dtype, asym, zp):
+    c = synth.make_case(0, K, N, G, dtype, asym=asym, seed=K + N, zp_bias=zp)
+    t = case_tensors(c)
+    wt = w.w4a16_dequant(t["b_q"], t["scales"], t["qzeros"], G, zp)
+    torch.cuda.synchronize()
+    assert np.array_equal(torch_to_bits(wt), oracle.dequant_t(c.b_q, c.scales, c.qzeros, G, zp, dtype))
+
+
+# ------------------------------------------------------------------------------------------------
+# the product
+# ------------------------------------------------------------------------------------------------
+SMALL_CASES = [
+    # (M, K, N, G, dtype, asym, bias)
+    (4, 256, 512, 128, "f16", False, False),      # the pages' fake-impl shape
+    (1, 1152, 4224, 32, "bf16", False, False),    # 2112-model gate+up
+    (5, 2112, 1152, 32, "bf16", False, False),    # 2112-model down
+    (8, 2560, 3840, 128, "f16", True, True),      # 4B-class
+    (9, 512, 8320, 64, "bf16", True, False),      # M just past 8, ragged column tile
+    (16, 1024, 4096, 128, "f16", False, True),
+    (33, 768, 2048, 64, "bf16", True, True),      # several row tiles, ragged last
+    (64, 512, 1056, 32, "f16", True, False),      # N % 64 != 0
+    (3, 4096, 96, 4096, "bf16", False, False),    # per-channel, narrow N
+    (7, 100, 520, 100, "f16", True, True),        # K and N off every fast-path alignment
+    (130, 256, 640, 128, "bf16", True, True),     # prefill-sized M, several tiles
+]
+
+
+@pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: "M%d_K%d_N%d_G%d_%s_%s%s" % (
+    c[0], c[1], c[2], c[3], c[4], "asym" if c[5] else "sym", "_bias" if c[6] else ""))
+def test_gemm_matches_oracle_every_path(w, case):
+    M, K, N, G, dtype, asym, bias = case
+    c = synth.make_case(M, K, N, G, dtype, asym=asym, bias=bias, seed=M * 7 + K + N)
+    paths, auto = supported_paths(w, c)
+    outs = {}
+    for p in paths + [None]:
+        outs[p] = run(w, c, p)
+        check_against_oracle(c, outs[p], label=f"path={p or auto}")
+    # the automatic choice is one of the checked paths and gives the same bits as forcing it
+    assert np.array_equal(outs[None], outs[auto])
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M,K,N,G", [(8, 1024, 2048, 128), (1, 2112, 1152, 32), (64, 512, 512, 64)])
+def test_identity_a_is_bitexact_dequant(w, dtype, M, K, N, G):
+    c = synth.make_case(M, K, N, G, dtype, asym=True, seed=3 + M)
+    rng = np.random.default_rng(M)
+    ks = rng.choice(K, size=M, replace=False)
+    one = int(oracle.ieee.t_encode_rne(np.array([1.0]), dtype)[0])
+    c.a[:] = 0
+    c.a[np.arange(M), ks] = one
+    want = oracle.dequant_t(c.b_q, c.scales, c.qzeros, G, 8, dtype)[ks]
+    for p in supported_paths(w, c)[0]:
+        got = run(w, c, p)
+        assert np.array_equal(got, want), f"path {p}: {int((got != want).sum())} differing outputs"
+
+
+def test_m_zero_touches_nothing(w):
+    c = synth.make_case(0, 256, 512, 128, "f16", seed=1)
+    t = case_tensors(c)
+    before = w.w4a16_debug_launch_count()
+    out = w.w4a16_gemm(t["a"], t["b_q"], t["scales"], None, 128)
+    assert out.shape == (0, 512)
+    assert w.w4a16_debug_launch_count() == before
+
+
+def test_deterministic_and_writes_only_out(w):
+    for M, K, N, G, asym in [(5, 2112, 1152, 32, False), (8, 2560, 3840, 128, True), (40, 512, 2048, 64, True)]:
+        c = synth.make_case(M, K, N, G, "bf16", asym=asym, bias=True, seed=M)
+        for p in supported_paths(w, c)[0]:
+            t = case_tensors(c)
+            buf = torch.full((M * N + 4096,), float("nan"), dtype=torch.bfloat16, device="cuda")
+            canary = torch_to_bits(buf[M * N:])
+            out = buf[:M * N].view(M, N)
+            with forced_path(p):
+                w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"], out=out)
+                first = torch_to_bits(out).copy()
+                w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"], out=out)
+            torch.cuda.synchronize()
+            assert not np.isnan(oracle.ieee.t_decode(first, "bf16")).any(), f"{p}: unwritten outputs"
+            assert np.array_equal(first, torch_to_bits(out)), f"{p}: not deterministic"
+            assert np.array_equal(canary, torch_to_bits(buf[M * N:])), f"{p}: wrote past out"
+
+
+def test_unaligned_pointers_take_the_generic_path(w):
+    c = synth.make_case(4, 512, 1024, 128, "f16", asym=True, bias=True, seed=5)
+    t = case_tensors(c)
+    a2 = torch.empty(c.M * c.K + 1, dtype=torch.float16, device="cuda")[1:].view(c.M, c.K)
+    a2.copy_(t["a"])
+    out = w.w4a16_gemm(a2, t["b_q"], t["scales"], t["qzeros"], c.G, 8, t["bias"])
+    torch.cuda.synchronize()
+    check_against_oracle(c, torch_to_bits(out), label="unaligned a")
+
+
+@pytest.mark.parametrize("zp", [0, 15])
+def test_zp_bias_values(w, zp):
+    c = synth.make_case(3, 512, 512, 64, "f16", seed=zp, zp_bias=zp)
+    for p in supported_paths(w, c)[0]:
+        check_against_oracle(c, run(w, c, p), label=f"zp_bias={zp} path={p}")
+
+
+def test_dispatch_threshold_neighbours(w):
+    # every switch point of the dispatcher, +-1
+    for M in (1, 8, 9, 16, 17, 64, 65, 128, 129):
+        c = synth.make_case(M, 512, 1024, 128, "bf16", asym=True, seed=M)
+        check_against_oracle(c, run(w, c), label=f"M={M}")
+
+
+# ------------------------------------------------------------------------------------------------
+# the measurement workloads at full size
+# ------------------------------------------------------------------------------------------------
+def _config_ids(name):
+    return [f"{name}-M{M}-K{K}-N{N}-G{G}-{dt}-{'asym' if asym else 'sym'}"
+            for (M, K, N, G, dt, asym, bias, lo, hi, seed) in synth.config_cases(name)]
+
+
+@pytest.mark.parametrize("args", list(synth.config_cases("tiny")) + list(synth.config_cases("decode_2112")),
+                         ids=_config_ids("tiny") + _config_ids("decode_2112"))
+def test_decode_workloads_full_output(w, args):
+    M, K, N, G, dt, asym, bias, lo, hi, seed = args
+    c = synth.make_case(M, K, N, G, dt, asym=asym, bias=bias, seed=seed, scale_lo=lo, scale_hi=hi)
+    check_against_oracle(c, run(w, c), label="full")
+
+
+@pytest.mark.parametrize("args", list(synth.config_cases("decode_4b")), ids=_config_ids("decode_4b"))
+def test_decode_4b_workload_sampled_columns(w, args):
+    M, K, N, G, dt, asym, bias, lo, hi, seed = args
+    c = synth.make_case(M, K, N, G, dt, asym=asym, bias=bias, seed=seed, scale_lo=lo, scale_hi=hi)
+    out = run(w, c)
+    cols = sample_cols(N, np.random.default_rng(seed))
+    check_against_oracle(c, out, cols=cols, label="sampled")

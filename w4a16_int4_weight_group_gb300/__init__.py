@@ -1,0 +1,223 @@
+"""Python binding of libw4a16.so (the W4A16 linear layer on GB300): argument marshalling only.
+
+Every function here checks tensor devices, dtypes and shapes, takes raw device pointers and the
+current CUDA stream from PyTorch, and calls the C entry point of the same name. All computation runs
+in the library's CUDA kernels; there is no fallback. If the shared library is missing the import of
+the ``lib`` handle fails loudly: build it with ``python -m w4a16_int4_weight_group_gb300.build``.
+
+The facade mirrors ``triton_w4a16_gemm(a, b_q, scales, qzeros, group_size, zp_bias=8)`` from the
+PR #51453 report (key source snippets), extended by ``bias`` and an optional ``out``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libw4a16.so")
+
+W4A16_F16, W4A16_BF16 = 0, 1
+STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4: "CUDA", 5: "TIMEOUT"}
+PATHS = {0: "none", 1: "generic", 2: "decode", 3: "prefill"}
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("words_per_lane", ctypes.c_int32), ("m_tile", ctypes.c_int32),
+                ("n_tile", ctypes.c_int32), ("k_split", ctypes.c_int32), ("warps", ctypes.c_int32),
+                ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+    def as_dict(self):
+        d = {f: getattr(self, f) for f, _ in self._fields_}
+        d["path_name"] = PATHS.get(self.path, str(self.path))
+        return d
+
+
+_lib = None
+_c_i64, _c_int, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+
+# (name, restype, argtypes) of every entry point declared in include/w4a16.h
+SIGNATURES = [
+    ("w4a16_pack", _c_int, [_vp, _vp, _c_i64, _c_i64, _vp]),
+    ("w4a16_unpack", _c_int, [_vp, _vp, _c_i64, _c_i64, _vp]),
+    ("w4a16_dequant", _c_int, [_vp, _vp, _vp, _c_i64, _c_i64, _c_int, _c_int, _c_int, _vp, _vp]),
+    ("w4a16_gemm", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_int, _vp]),
+    ("w4a16_can_implement", _c_int, [_c_i64, _c_i64, _c_int, _c_int, _c_int]),
+    ("w4a16_plan", _c_int, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(Plan)]),
+    ("w4a16_last_error", ctypes.c_char_p, []),
+    ("w4a16_get_device_error", _c_int, []),
+    ("w4a16_debug_selected_path", _c_int, [_c_i64, _c_i64, _c_i64, _c_int]),
+    ("w4a16_debug_set_wait_limit_ns", _c_int, [ctypes.c_uint64]),
+    ("w4a16_debug_launch_count", ctypes.c_uint64, []),
+    ("w4a16_version", ctypes.c_char_p, []),
+]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libw4a16.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m w4a16_int4_weight_group_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, res, args in SIGNATURES:
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().w4a16_last_error().decode()
+
+
+def _check(status: int):
+    if status != 0:
+        raise W4A16Error(status, last_error())
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float16:
+        return W4A16_F16
+    if dt == torch.bfloat16:
+        return W4A16_BF16
+    raise W4A16Error(2, f"Only float16/bfloat16 activations are supported (got {dt})")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _require_cuda(*ts):
+    dev = None
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous (row-major)")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("all tensors must be on the same device")
+    return dev
+
+
+def w4a16_pack(q: torch.Tensor, packed: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """uint8 [rows, n] (values 0..15) -> int32 [rows, n/8]; nibble j of word c <- column 8c+j."""
+    if q.dtype != torch.uint8 or q.dim() != 2:
+        raise ValueError("q must be a 2-D uint8 tensor")
+    rows, n = q.shape
+    if packed is None:
+        packed = torch.empty((rows, n // 8), dtype=torch.int32, device=q.device)
+    dev = _require_cuda(q, packed)
+    _check(lib().w4a16_pack(_ptr(q), _ptr(packed), rows, n, _stream(dev)))
+    return packed
+
+
+def w4a16_unpack(packed: torch.Tensor, n: Optional[int] = None, q: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """int32 [rows, n/8] -> uint8 [rows, n]."""
+    if packed.dtype != torch.int32 or packed.dim() != 2:
+        raise ValueError("packed must be a 2-D int32 tensor")
+    rows = packed.shape[0]
+    n = packed.shape[1] * 8 if n is None else n
+    if q is None:
+        q = torch.empty((rows, n), dtype=torch.uint8, device=packed.device)
+    dev = _require_cuda(q, packed)
+    _check(lib().w4a16_unpack(_ptr(packed), _ptr(q), rows, n, _stream(dev)))
+    return q
+
+
+def w4a16_dequant(b_q: torch.Tensor, scales: torch.Tensor, qzeros: Optional[torch.Tensor], group_size: int,
+                  zp_bias: int = 8, w_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """dequant(W)[k, n] = RNE_dtype((q - zp) * scale) as a [K, N] tensor of the scales' dtype."""
+    k, nw = b_q.shape
+    n = nw * 8
+    if w_out is None:
+        w_out = torch.empty((k, n), dtype=scales.dtype, device=b_q.device)
+    dev = _require_cuda(b_q, scales, qzeros, w_out)
+    _check(lib().w4a16_dequant(_ptr(b_q), _ptr(scales), _ptr(qzeros), k, n, group_size, zp_bias,
+                               _dtype_code(scales.dtype), _ptr(w_out), _stream(dev)))
+    return w_out
+
+
+def w4a16_gemm(a: torch.Tensor, b_q: torch.Tensor, scales: torch.Tensor, qzeros: Optional[torch.Tensor],
+               group_size: int, zp_bias: int = 8, bias: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """out[M, N] = cast(a[M, K] @ dequant(b_q, scales, qzeros|zp_bias) + bias), fp32 accumulation.
+
+    Output shape (M, b_q.shape[1] * 8), dtype and device of ``a`` (PR #51453 report, fake impl).
+    """
+    if a.dim() != 2 or b_q.dim() != 2:
+        raise ValueError("a and b_q must be 2-D")
+    m, k = a.shape
+    n = b_q.shape[1] * 8
+    if b_q.shape[0] != k:
+        raise ValueError(f"b_q has {b_q.shape[0]} rows, a has K={k}")
+    if out is None:
+        out = torch.empty((m, n), dtype=a.dtype, device=a.device)
+    dev = _require_cuda(a, b_q, scales, qzeros, bias, out)
+    if scales.dtype != a.dtype or out.dtype != a.dtype or (bias is not None and bias.dtype != a.dtype):
+        raise ValueError("scales, bias and out must have the dtype of a")
+    if b_q.dtype != torch.int32 or (qzeros is not None and qzeros.dtype != torch.int32):
+        raise ValueError("b_q and qzeros must be int32")
+    _check(lib().w4a16_gemm(_ptr(a), _ptr(b_q), _ptr(scales), _ptr(qzeros), group_size, zp_bias, _ptr(bias),
+                            _ptr(out), m, k, n, _dtype_code(a.dtype), _stream(dev)))
+    return out
+
+
+def w4a16_can_implement(k: int, n: int, group_size: int, dtype, has_g_idx: bool = False):
+    """(True, "") or (False, reason), like the pages' can_implement."""
+    code = dtype if isinstance(dtype, int) else ({torch.float16: 0, torch.bfloat16: 1}.get(dtype, 99))
+    st = lib().w4a16_can_implement(k, n, group_size, code, int(bool(has_g_idx)))
+    return (True, "") if st == 0 else (False, last_error())
+
+
+def w4a16_plan(m: int, k: int, n: int, group_size: int, dtype=W4A16_F16, has_zp: bool = False,
+               num_sms: int = 0) -> dict:
+    p = Plan()
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    _check(lib().w4a16_plan(m, k, n, group_size, code, int(bool(has_zp)), num_sms, ctypes.byref(p)))
+    return p.as_dict()
+
+
+def w4a16_get_device_error() -> int:
+    return lib().w4a16_get_device_error()
+
+
+def w4a16_debug_selected_path(m: int, k: int, n: int, group_size: int) -> int:
+    return lib().w4a16_debug_selected_path(m, k, n, group_size)
+
+
+def w4a16_debug_set_wait_limit_ns(ns: int):
+    _check(lib().w4a16_debug_set_wait_limit_ns(ns))
+
+
+def w4a16_debug_launch_count() -> int:
+    return int(lib().w4a16_debug_launch_count())
+
+
+def w4a16_version() -> str:
+    return lib().w4a16_version().decode()
+
+
+__all__ = ["w4a16_pack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_can_implement", "w4a16_plan",
+           "w4a16_get_device_error", "w4a16_debug_selected_path", "w4a16_debug_set_wait_limit_ns",
+           "w4a16_debug_launch_count", "w4a16_version", "W4A16Error", "lib", "last_error", "LIB_PATH",
+           "SIGNATURES", "PATHS"]

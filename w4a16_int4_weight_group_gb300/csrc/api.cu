@@ -1,0 +1,327 @@
+// C ABI of libw4a16.so: argument validation, the runtime dispatcher and the entry points.
+//
+// Validation mirrors TritonW4A16LinearKernel.can_implement (PR #43731 report, key source snippets):
+// fp16/bf16 activations only, N % 8 == 0 ("8 int4 values packed per int32"), no activation
+// reordering, group size in the supported list or equal to K. The tile / split-K / cluster choice is
+// made on every call from the runtime M, K, N, G and the device, inside the library: the PR #51453
+// report (motivation) traces a decode throughput regression to a compiler freezing the Python tile
+// selection of the prefill shape into decode calls.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+
+namespace w4a16 {
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+
+w4a16_status fail(w4a16_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+w4a16_status ok() {
+  g_last_error.clear();
+  return W4A16_OK;
+}
+
+w4a16_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(W4A16_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+Range range(const void *p, int64_t bytes) {
+  const auto lo = reinterpret_cast<uintptr_t>(p);
+  return {lo, lo + static_cast<uintptr_t>(bytes)};
+}
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+constexpr int64_t kMaxDim = int64_t(1) << 31;
+constexpr int64_t kMaxN = int64_t(1) << 24;  // column tiles index a grid dimension of at most 65535
+
+bool group_size_ok(int G, int64_t K) { return G == 32 || G == 64 || G == 128 || int64_t(G) == K; }
+
+// Shared rules of w4a16_can_implement / w4a16_dequant / w4a16_gemm (host only, no device access).
+w4a16_status check_config(int64_t K, int64_t N, int G, int dtype) {
+  if (dtype != W4A16_F16 && dtype != W4A16_BF16)
+    return fail(W4A16_ERR_UNSUPPORTED, "Only float16/bfloat16 activations are supported (dtype %d)", dtype);
+  if (K <= 0 || N <= 0 || K >= kMaxDim || N > kMaxN)
+    return fail(W4A16_ERR_INVALID_ARG, "K (%lld) must be in [1, 2^31) and N (%lld) in [1, 2^24]",
+                (long long)K, (long long)N);
+  if (N % 8 != 0)
+    return fail(W4A16_ERR_INVALID_ARG,
+                "Output features (%lld) must be divisible by 8 (8 int4 values packed per int32)",
+                (long long)N);
+  if (!group_size_ok(G, K))
+    return fail(W4A16_ERR_UNSUPPORTED, "Group size %d not supported; supported: [32, 64, 128] or K (%lld)",
+                G, (long long)K);
+  if (K % G != 0)
+    return fail(W4A16_ERR_INVALID_ARG, "K (%lld) must be a multiple of group_size (%d)", (long long)K, G);
+  return W4A16_OK;
+}
+
+// W4A16_FORCE_PATH=generic|decode|prefill restricts the dispatcher (tests and benchmarks only).
+int forced_path() {
+  const char *s = std::getenv("W4A16_FORCE_PATH");
+  if (!s || !*s) return -1;
+  if (!std::strcmp(s, "generic")) return W4A16_PATH_GENERIC;
+  if (!std::strcmp(s, "decode")) return W4A16_PATH_DECODE;
+  if (!std::strcmp(s, "prefill")) return W4A16_PATH_PREFILL;
+  return -1;
+}
+
+// M at and above which the tcgen05 path is preferred when it applies.
+constexpr int64_t kPrefillMinM = 65;
+
+void choose_plan(const GemmArgs &g, int num_sms, w4a16_plan_t *p) {
+  std::memset(p, 0, sizeof(*p));
+  if (g.M == 0) {
+    p->path = W4A16_PATH_NONE;
+    return;
+  }
+  // the decode grid indexes row tiles of up to 32 rows in a dimension of at most 65535
+  const bool dec = decode_supported(g) && (g.M + 31) / 32 <= 65535;
+  const bool pre = prefill_supported(g);
+  const int force = forced_path();
+  int path;
+  if (force == W4A16_PATH_GENERIC || (!dec && !pre)) {
+    path = W4A16_PATH_GENERIC;
+  } else if (force == W4A16_PATH_DECODE && dec) {
+    path = W4A16_PATH_DECODE;
+  } else if (force == W4A16_PATH_PREFILL && pre) {
+    path = W4A16_PATH_PREFILL;
+  } else if (pre && (g.M >= kPrefillMinM || !dec)) {
+    path = W4A16_PATH_PREFILL;
+  } else if (dec) {
+    path = W4A16_PATH_DECODE;
+  } else {
+    path = W4A16_PATH_GENERIC;
+  }
+  if (path == W4A16_PATH_DECODE) {
+    decode_make_plan(g.M, g.K, g.N, g.qzeros != nullptr, num_sms, p);
+  } else if (path == W4A16_PATH_PREFILL) {
+    prefill_make_plan(g.M, g.K, g.N, g.group_size, num_sms, p);
+  } else {
+    p->path = W4A16_PATH_GENERIC;
+    p->m_tile = 8;
+    p->n_tile = 256;
+    p->k_split = 1;
+    p->warps = 8;
+    p->grid = ((g.M + 7) / 8) * ((g.N / 8 + 31) / 32);
+  }
+}
+
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+cudaError_t current_device_info(DeviceInfo *info) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool have[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && have[dev]) {
+    *info = cache[dev];
+    return cudaSuccess;
+  }
+  DeviceInfo d{};
+  d.device = dev;
+  if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+      cudaSuccess)
+    return e;
+  if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) {
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *info = d;
+  return cudaSuccess;
+}
+
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+const char *w4a16_version(void) { return "w4a16-gb300 0.1.0 (sm_103a)"; }
+
+const char *w4a16_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t w4a16_debug_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+w4a16_status w4a16_can_implement(int64_t k, int64_t n, int group_size, int dtype, int has_g_idx) {
+  if (dtype != W4A16_F16 && dtype != W4A16_BF16)
+    return fail(W4A16_ERR_UNSUPPORTED, "Only float16/bfloat16 activations are supported (dtype %d)", dtype);
+  if (n > 0 && n % 8 != 0)
+    return fail(W4A16_ERR_INVALID_ARG,
+                "Output features (%lld) must be divisible by 8 (8 int4 values packed per int32)",
+                (long long)n);
+  if (has_g_idx)
+    return fail(W4A16_ERR_UNSUPPORTED, "Activation reordering (g_idx) is not supported");
+  const w4a16_status st = check_config(k, n, group_size, dtype);
+  if (st != W4A16_OK) return st;
+  return ok();
+}
+
+w4a16_status w4a16_pack(const uint8_t *q, int32_t *packed, int64_t rows, int64_t n,
+                        w4a16_stream_t stream) {
+  if (rows < 0 || n <= 0 || rows >= kMaxDim || n >= kMaxDim)
+    return fail(W4A16_ERR_INVALID_ARG, "rows (%lld) must be >= 0 and n (%lld) > 0", (long long)rows,
+                (long long)n);
+  if (n % 8) return fail(W4A16_ERR_INVALID_ARG, "n (%lld) must be divisible by 8", (long long)n);
+  if (rows == 0) return ok();
+  if (!q || !packed) return fail(W4A16_ERR_INVALID_ARG, "q and packed must not be NULL");
+  if (!aligned(packed, 4)) return fail(W4A16_ERR_MISALIGNED, "packed must be 4-byte aligned");
+  if (overlaps(range(q, rows * n), range(packed, rows * n / 2)))
+    return fail(W4A16_ERR_INVALID_ARG, "q and packed overlap");
+  const cudaError_t e = launch_pack(q, packed, rows, n, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "w4a16_pack launch");
+  return ok();
+}
+
+w4a16_status w4a16_unpack(const int32_t *packed, uint8_t *q, int64_t rows, int64_t n,
+                          w4a16_stream_t stream) {
+  if (rows < 0 || n <= 0 || rows >= kMaxDim || n >= kMaxDim)
+    return fail(W4A16_ERR_INVALID_ARG, "rows (%lld) must be >= 0 and n (%lld) > 0", (long long)rows,
+                (long long)n);
+  if (n % 8) return fail(W4A16_ERR_INVALID_ARG, "n (%lld) must be divisible by 8", (long long)n);
+  if (rows == 0) return ok();
+  if (!q || !packed) return fail(W4A16_ERR_INVALID_ARG, "q and packed must not be NULL");
+  if (!aligned(packed, 4)) return fail(W4A16_ERR_MISALIGNED, "packed must be 4-byte aligned");
+  if (overlaps(range(q, rows * n), range(packed, rows * n / 2)))
+    return fail(W4A16_ERR_INVALID_ARG, "q and packed overlap");
+  const cudaError_t e = launch_unpack(packed, q, rows, n, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "w4a16_unpack launch");
+  return ok();
+}
+
+w4a16_status w4a16_dequant(const int32_t *b_q, const void *scales, const int32_t *qzeros, int64_t k,
+                           int64_t n, int group_size, int zp_bias, w4a16_dtype dtype, void *w_out,
+                           w4a16_stream_t stream) {
+  w4a16_status st = check_config(k, n, group_size, dtype);
+  if (st != W4A16_OK) return st;
+  if (!qzeros && (zp_bias < 0 || zp_bias > 15))
+    return fail(W4A16_ERR_INVALID_ARG, "zp_bias (%d) must be in [0, 15]", zp_bias);
+  if (!b_q || !scales || !w_out) return fail(W4A16_ERR_INVALID_ARG, "b_q, scales and w_out must not be NULL");
+  if (!aligned(b_q, 4) || !aligned(scales, 2) || !aligned(w_out, 2) || (qzeros && !aligned(qzeros, 4)))
+    return fail(W4A16_ERR_MISALIGNED, "tensors must be naturally aligned");
+  const Range wo = range(w_out, k * n * 2);
+  if (overlaps(wo, range(b_q, k * n / 2)) || overlaps(wo, range(scales, (k / group_size) * n * 2)) ||
+      (qzeros && overlaps(wo, range(qzeros, (k / group_size) * n / 2))))
+    return fail(W4A16_ERR_INVALID_ARG, "w_out overlaps an input");
+  const cudaError_t e = launch_dequant(b_q, scales, qzeros, k, n, group_size, zp_bias, dtype, w_out,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "w4a16_dequant launch");
+  return ok();
+}
+
+static w4a16_status validate_gemm(const GemmArgs &g) {
+  w4a16_status st = check_config(g.K, g.N, g.group_size, g.dtype);
+  if (st != W4A16_OK) return st;
+  if (g.M < 0 || g.M >= kMaxDim) return fail(W4A16_ERR_INVALID_ARG, "M (%lld) must be in [0, 2^31)", (long long)g.M);
+  if (!g.qzeros && (g.zp_bias < 0 || g.zp_bias > 15))
+    return fail(W4A16_ERR_INVALID_ARG, "zp_bias (%d) must be in [0, 15]", g.zp_bias);
+  if (g.M == 0) return W4A16_OK;
+  if (!g.a || !g.b_q || !g.scales || !g.out)
+    return fail(W4A16_ERR_INVALID_ARG, "a, b_q, scales and out must not be NULL");
+  if (!aligned(g.a, 2) || !aligned(g.b_q, 4) || !aligned(g.scales, 2) || !aligned(g.out, 2) ||
+      (g.qzeros && !aligned(g.qzeros, 4)) || (g.bias && !aligned(g.bias, 2)))
+    return fail(W4A16_ERR_MISALIGNED, "tensors must be naturally aligned (2 bytes for 16-bit, 4 for int32)");
+  const int64_t ng = g.K / g.group_size;
+  const Range o = range(g.out, g.M * g.N * 2);
+  if (overlaps(o, range(g.a, g.M * g.K * 2)) || overlaps(o, range(g.b_q, g.K * g.N / 2)) ||
+      overlaps(o, range(g.scales, ng * g.N * 2)) || (g.qzeros && overlaps(o, range(g.qzeros, ng * g.N / 2))) ||
+      (g.bias && overlaps(o, range(g.bias, g.N * 2))))
+    return fail(W4A16_ERR_INVALID_ARG, "out overlaps an input tensor");
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_gemm(const void *a, const int32_t *b_q, const void *scales, const int32_t *qzeros,
+                        int group_size, int zp_bias, const void *bias, void *out, int64_t m,
+                        int64_t k, int64_t n, w4a16_dtype dtype, w4a16_stream_t stream) {
+  GemmArgs g{a, b_q, scales, qzeros, group_size, zp_bias, bias, out, m, k, n, static_cast<int>(dtype),
+             reinterpret_cast<cudaStream_t>(stream)};
+  w4a16_status st = validate_gemm(g);
+  if (st != W4A16_OK) return st;
+  if (m == 0) return ok();
+  DeviceInfo dev;
+  cudaError_t e = current_device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  w4a16_plan_t plan;
+  choose_plan(g, dev.num_sms, &plan);
+  switch (plan.path) {
+    case W4A16_PATH_DECODE: e = launch_gemm_decode(g, plan); break;
+    case W4A16_PATH_PREFILL: e = launch_gemm_prefill(g, plan); break;
+    default: e = launch_gemm_generic(g); break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "w4a16_gemm launch");
+  return ok();
+}
+
+w4a16_status w4a16_plan(int64_t m, int64_t k, int64_t n, int group_size, int dtype, int has_zp,
+                        int num_sms, w4a16_plan_t *plan) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan must not be NULL");
+  w4a16_status st = check_config(k, n, group_size, dtype);
+  if (st != W4A16_OK) return st;
+  if (m < 0 || m >= kMaxDim) return fail(W4A16_ERR_INVALID_ARG, "M (%lld) must be in [0, 2^31)", (long long)m);
+  if (num_sms <= 0) {
+    DeviceInfo dev;
+    cudaError_t e = current_device_info(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    num_sms = dev.num_sms;
+  }
+  // Pointers are assumed 16-byte aligned: any 16-byte aligned address stands in for them.
+  static const int32_t kAlignedWord[4] = {0, 0, 0, 0};
+  const void *p16 = reinterpret_cast<const void *>(
+      (reinterpret_cast<uintptr_t>(kAlignedWord) + 15) & ~uintptr_t(15));
+  GemmArgs g{p16, static_cast<const int32_t *>(p16), p16, has_zp ? static_cast<const int32_t *>(p16) : nullptr,
+             group_size, 8, nullptr, nullptr, m, k, n, dtype, nullptr};
+  choose_plan(g, num_sms, plan);
+  return ok();
+}
+
+int w4a16_debug_selected_path(int64_t m, int64_t k, int64_t n, int group_size) {
+  w4a16_plan_t p;
+  if (w4a16_plan(m, k, n, group_size, W4A16_F16, 0, 0, &p) != W4A16_OK) return -1;
+  return p.path;
+}
+
+w4a16_status w4a16_get_device_error(void) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "synchronise");
+  uint32_t err = 0;
+  e = prefill_take_device_error(&err);
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  if (err) return fail(W4A16_ERR_TIMEOUT, "a bounded device-side wait gave up (code 0x%x)", err);
+  return ok();
+}
+
+w4a16_status w4a16_debug_set_wait_limit_ns(uint64_t ns) {
+  const cudaError_t e = prefill_set_wait_limit_ns(ns);
+  if (e != cudaSuccess) return cuda_fail(e, "set wait limit");
+  return ok();
+}
+
+}  // extern "C"

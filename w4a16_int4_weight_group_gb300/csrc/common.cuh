@@ -1,0 +1,144 @@
+// Device-side helpers shared by the kernels of libw4a16.so: dtype tags, inline-PTX wrappers for
+// byte permutes, packed 16-bit arithmetic with explicit rounding, warp-level MMA, cp.async,
+// thread-block-cluster barriers and distributed shared memory.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+namespace w4a16 {
+
+// ---------------------------------------------------------------------------------------------
+// dtype tags
+// ---------------------------------------------------------------------------------------------
+struct F16 {
+  using T = __half;
+  static constexpr bool kBF16 = false;
+  __device__ static __forceinline__ float to_float(T x) { return __half2float(x); }
+  __device__ static __forceinline__ T from_float_rn(float x) { return __float2half_rn(x); }
+};
+struct BF16 {
+  using T = __nv_bfloat16;
+  static constexpr bool kBF16 = true;
+  __device__ static __forceinline__ float to_float(T x) { return __bfloat162float(x); }
+  __device__ static __forceinline__ T from_float_rn(float x) { return __float2bfloat16_rn(x); }
+};
+
+__device__ __forceinline__ float bits_to_float(uint16_t b, bool is_bf16) {
+  return is_bf16 ? __uint_as_float(uint32_t(b) << 16) : __half2float(__ushort_as_half(b));
+}
+
+// ---------------------------------------------------------------------------------------------
+// integer bit manipulation
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// (a & mask) | bits, one LOP3 (truth table 0xEA for (A & B) | C)
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t bits) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));
+  return d;
+}
+
+// ---------------------------------------------------------------------------------------------
+// packed 16-bit arithmetic, round-to-nearest-even made explicit (no contraction into FMA)
+// ---------------------------------------------------------------------------------------------
+template <bool BF>
+__device__ __forceinline__ uint32_t sub2_rn(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (BF) asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <bool BF>
+__device__ __forceinline__ uint32_t mul2_rn(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (BF) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// ---------------------------------------------------------------------------------------------
+// warp-level MMA m16n8k16, fp32 accumulate: D = A(16x16, row) * B(16x8, col) + D
+// ---------------------------------------------------------------------------------------------
+template <bool BF>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  if constexpr (BF) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// shared memory addressing, cp.async (16-byte, L2-only caching, optional zero fill)
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// Copies 16 bytes global -> shared. When `valid` is false nothing is read and 16 zero bytes are
+// written (src-size 0); `src` must still be a valid address.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void lds64(uint32_t addr, uint32_t &x, uint32_t &y) {
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(x), "=r"(y) : "r"(addr));
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t x;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x) : "r"(addr));
+  return x;
+}
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t &x, uint32_t &y, uint32_t &z,
+                                       uint32_t &w) {
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(x), "=r"(y), "=r"(z), "=r"(w)
+               : "r"(addr));
+}
+
+// ---------------------------------------------------------------------------------------------
+// thread-block clusters: hardware barrier and distributed shared memory reads
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Maps a shared::cta address of this CTA to the same offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+}  // namespace w4a16

@@ -1,0 +1,59 @@
+// Host-side interfaces between the translation units of libw4a16.so (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/w4a16.h"
+
+namespace w4a16 {
+
+struct GemmArgs {
+  const void *a;
+  const int32_t *b_q;
+  const void *scales;
+  const int32_t *qzeros;  // may be null
+  int group_size;
+  int zp_bias;
+  const void *bias;  // may be null
+  void *out;
+  int64_t M, K, N;
+  int dtype;  // w4a16_dtype
+  cudaStream_t stream;
+};
+
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int max_smem_optin;  // bytes of dynamic shared memory a CTA may opt into
+  int cc_major, cc_minor;
+};
+
+// Cached per-device properties of the current device (queried once per device).
+cudaError_t current_device_info(DeviceInfo *info);
+
+// Records one kernel launch in the process-wide counter.
+void note_launch();
+
+cudaError_t launch_pack(const uint8_t *q, int32_t *packed, int64_t rows, int64_t n, cudaStream_t s);
+cudaError_t launch_unpack(const int32_t *packed, uint8_t *q, int64_t rows, int64_t n, cudaStream_t s);
+cudaError_t launch_dequant(const int32_t *b_q, const void *scales, const int32_t *qzeros, int64_t k,
+                           int64_t n, int group_size, int zp_bias, int dtype, void *w_out,
+                           cudaStream_t s);
+
+cudaError_t launch_gemm_generic(const GemmArgs &g);
+
+// Decode path: plan fields words_per_lane, m_tile, k_split, warps are honoured.
+bool decode_supported(const GemmArgs &g);
+void decode_make_plan(int64_t M, int64_t K, int64_t N, int has_zp, int num_sms, w4a16_plan_t *p);
+cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &p);
+
+// Prefill path (tcgen05).
+bool prefill_supported(const GemmArgs &g);
+void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, w4a16_plan_t *p);
+cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &p);
+// Reads and clears the device error word of the prefill kernels on the current device.
+cudaError_t prefill_take_device_error(uint32_t *err);
+cudaError_t prefill_set_wait_limit_ns(uint64_t ns);
+
+}  // namespace w4a16

@@ -1,0 +1,104 @@
+// Layout kernels: pack / unpack of 4-bit values eight per int32 along the last dimension, and the
+// materialised dequantisation W[k, n] = RNE_dtype((q - zp) * s).
+//
+// Packing: nibble j (bits 4j..4j+3) of word c holds column 8c+j - the plain reading of "eight values
+// packed along N" (PR #51453 report, implementation breakdown: N = b_q.shape[1] * 8).
+// Dequantisation: (raw - zero_point) * scale with group rows along K (PR #40977 report, key source
+// snippets, test reference).
+#include "common.cuh"
+#include "internal.h"
+
+namespace w4a16 {
+namespace {
+
+constexpr int kThreads = 256;
+
+int grid_for(int64_t items) {
+  int64_t blocks = (items + kThreads - 1) / kThreads;
+  if (blocks > 65535LL * 16) blocks = 65535LL * 16;  // grid-stride loops cover the rest
+  return static_cast<int>(blocks < 1 ? 1 : blocks);
+}
+
+__global__ void pack_kernel(const uint8_t *__restrict__ q, int32_t *__restrict__ packed,
+                            int64_t words) {
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < words;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const uint8_t *src = q + i * 8;  // word i covers bytes [8i, 8i+8) of the row-major [rows, n]
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w |= uint32_t(src[j] & 0xF) << (4 * j);
+    packed[i] = static_cast<int32_t>(w);
+  }
+}
+
+__global__ void unpack_kernel(const int32_t *__restrict__ packed, uint8_t *__restrict__ q,
+                              int64_t words) {
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < words;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const uint32_t w = static_cast<uint32_t>(packed[i]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[i * 8 + j] = static_cast<uint8_t>((w >> (4 * j)) & 0xF);
+  }
+}
+
+template <class DT>
+__global__ void dequant_kernel(const int32_t *__restrict__ b_q, const uint16_t *__restrict__ scales,
+                               const int32_t *__restrict__ qzeros, int64_t K, int64_t N, int G,
+                               int zp_bias, uint16_t *__restrict__ w_out) {
+  using T = typename DT::T;
+  const int64_t nw = N / 8;
+  const int64_t words = K * nw;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < words;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t k = i / nw, c = i - k * nw;
+    const int64_t g = k / G;
+    const uint32_t w = static_cast<uint32_t>(b_q[i]);
+    const uint32_t z = qzeros ? static_cast<uint32_t>(qzeros[g * nw + c]) : 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int q = (w >> (4 * j)) & 0xF;
+      const int zp = qzeros ? int((z >> (4 * j)) & 0xF) : zp_bias;
+      const float s = bits_to_float(scales[g * N + c * 8 + j], DT::kBF16);
+      // (q - zp) is an integer in [-15, 15]: the fp32 product is exact, so this is one rounding.
+      const T v = DT::from_float_rn(float(q - zp) * s);
+      w_out[k * N + c * 8 + j] = *reinterpret_cast<const uint16_t *>(&v);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const uint8_t *q, int32_t *packed, int64_t rows, int64_t n, cudaStream_t s) {
+  const int64_t words = rows * (n / 8);
+  if (words == 0) return cudaSuccess;
+  pack_kernel<<<grid_for(words), kThreads, 0, s>>>(q, packed, words);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(const int32_t *packed, uint8_t *q, int64_t rows, int64_t n, cudaStream_t s) {
+  const int64_t words = rows * (n / 8);
+  if (words == 0) return cudaSuccess;
+  unpack_kernel<<<grid_for(words), kThreads, 0, s>>>(packed, q, words);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const int32_t *b_q, const void *scales, const int32_t *qzeros, int64_t k,
+                           int64_t n, int group_size, int zp_bias, int dtype, void *w_out,
+                           cudaStream_t s) {
+  const int64_t words = k * (n / 8);
+  if (words == 0) return cudaSuccess;
+  const auto *sc = static_cast<const uint16_t *>(scales);
+  auto *wo = static_cast<uint16_t *>(w_out);
+  if (dtype == W4A16_BF16)
+    dequant_kernel<BF16><<<grid_for(words), kThreads, 0, s>>>(b_q, sc, qzeros, k, n, group_size,
+                                                               zp_bias, wo);
+  else
+    dequant_kernel<F16><<<grid_for(words), kThreads, 0, s>>>(b_q, sc, qzeros, k, n, group_size,
+                                                              zp_bias, wo);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16
