@@ -118,6 +118,17 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t &x, uint32_t &y, 
 }
 
 // ---------------------------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream serialization may
+// start while the previous kernel of the stream is still running; griddep_wait() blocks until that
+// kernel has completed and its memory is visible (call it before the first global access), and
+// griddep_launch_dependents() lets the next kernel start launching. Both are no-ops otherwise.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
 // thread-block clusters: hardware barrier and distributed shared memory reads
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -87,7 +87,7 @@ struct DecodeParams {
 };
 
 template <class DT, int V, int J, bool HAS_ZP>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 2)
     decode_kernel(const DecodeParams p) {
   using L = DecodeLayout<V, J, HAS_ZP>;
   using T = typename DT::T;
@@ -117,48 +117,76 @@ __global__ void __launch_bounds__(kWarps * 32)
   uint8_t *ring = smem + warp * L::kWarpRing;
   const uint32_t ring_u32 = smem_u32(ring);
 
-  // ---- producer: issue the copies of local step i (k-step w_begin + i) into its slot ----
-  auto issue = [&](int i) {
-    if (i < nsteps) {
-      const int64_t ks = w_begin + i;
-      const uint32_t st = ring_u32 + (i % kRing) * L::kStage;
-      // packed weights: 16 rows x 2V chunks
+  // Inputs may be written by the previous kernel in the stream: wait for it before any global
+  // access, then let the next kernel start its launch while this one runs.
+  griddep_wait();
+  griddep_launch_dependents();
+
+  // ---- producer state: per-lane source pointers advanced by a fixed stride per k-step ----
+  // steps per scale group (G is a multiple of 16) and this warp's position inside its first group
+  const int spg = p.G / 16;
+  const int gpos0 = static_cast<int>(w_begin % spg);
+  const int64_t g_begin = w_begin / spg;
+  const int32_t *wsrc[V];
+  uint32_t wdst[V];
+  bool wok[V];
+#pragma unroll
+  for (int u = 0; u < V; ++u) {
+    const int ci = lane + 32 * u;
+    const int row = ci / (2 * V), c = ci % (2 * V);
+    const int64_t word = n0 / 8 + 4 * c;
+    wok[u] = word < NW;
+    wsrc[u] = p.b_q + (w_begin * 16 + row) * NW + (wok[u] ? word : 0);
+    wdst[u] = w_chunk_offset<V>(row, c);
+  }
+  constexpr int kAChunks = (2 * L::kMT + 31) / 32;
+  const uint16_t *asrc[kAChunks];
+  uint32_t adst[kAChunks];
+  bool aok[kAChunks], alane[kAChunks];
+#pragma unroll
+  for (int u = 0; u < kAChunks; ++u) {
+    const int ci = lane + 32 * u;
+    const int row = ci >> 1, c = ci & 1;
+    alane[u] = ci < 2 * L::kMT;
+    aok[u] = alane[u] && m0 + row < p.M;
+    asrc[u] = p.a + (aok[u] ? (m0 + row) * p.K + w_begin * 16 + 8 * c : 0);
+    adst[u] = L::kA + row * 32 + c * 16;
+  }
+  const bool s_lane = lane < L::kSBytes / 16;
+  const bool s_ok = s_lane && n0 + 8 * lane < p.N;
+  const uint16_t *ssrc = p.scales + g_begin * p.N + (s_ok ? n0 + 8 * lane : 0);
+  const bool z_lane = HAS_ZP && lane < L::kZBytes / 16;
+  const bool z_ok = z_lane && n0 / 8 + 4 * lane < NW;
+  const int32_t *zsrc = HAS_ZP ? p.qzeros + g_begin * NW + (z_ok ? n0 / 8 + 4 * lane : 0) : nullptr;
+  int issue_i = 0, issue_slot = 0, issue_gpos = gpos0;
+
+  // ---- producer: issue the copies of the next local step into its slot ----
+  auto issue = [&]() {
+    if (issue_i < nsteps) {
+      const uint32_t st = ring_u32 + issue_slot * L::kStage;
 #pragma unroll
       for (int u = 0; u < V; ++u) {
-        const int ci = lane + 32 * u;
-        const int row = ci / (2 * V), c = ci % (2 * V);
-        const int64_t word = n0 / 8 + 4 * c;
-        const bool ok = word < NW;
-        const int32_t *src = p.b_q + (ks * 16 + row) * NW + (ok ? word : 0);
-        cp_async_16(st + w_chunk_offset<V>(row, c), src, ok);
+        cp_async_16(st + wdst[u], wsrc[u], wok[u]);
+        wsrc[u] += 16 * NW;
       }
-      // activations: kMT rows x 2 chunks (16 halves)
 #pragma unroll
-      for (int u = 0; u < (2 * L::kMT + 31) / 32; ++u) {
-        const int ci = lane + 32 * u;
-        if (ci < 2 * L::kMT) {
-          const int row = ci >> 1, c = ci & 1;
-          const bool ok = m0 + row < p.M;
-          const uint16_t *src = p.a + (ok ? (m0 + row) * p.K + ks * 16 + 8 * c : 0);
-          cp_async_16(st + L::kA + row * 32 + c * 16, src, ok);
-        }
+      for (int u = 0; u < kAChunks; ++u) {
+        if (alane[u]) cp_async_16(st + adst[u], asrc[u], aok[u]);
+        if (aok[u]) asrc[u] += 16;
       }
-      // scales / zero points at group starts and at the first step of the warp
-      if (i == 0 || ((ks * 16) % p.G) == 0) {
-        const int64_t g = (ks * 16) / p.G;
-        if (lane < L::kSBytes / 16) {
-          const int64_t n = n0 + 8 * lane;
-          const bool ok = n < p.N;
-          cp_async_16(st + L::kS + 16 * lane, p.scales + g * p.N + (ok ? n : 0), ok);
-        }
+      if (issue_i == 0 || issue_gpos == 0) {
+        if (s_lane) cp_async_16(st + L::kS + 16 * lane, ssrc, s_ok);
         if constexpr (HAS_ZP) {
-          if (lane < L::kZBytes / 16) {
-            const int64_t word = n0 / 8 + 4 * lane;
-            const bool ok = word < NW;
-            cp_async_16(st + L::kZ + 16 * lane, p.qzeros + g * NW + (ok ? word : 0), ok);
-          }
+          if (z_lane) cp_async_16(st + L::kZ + 16 * lane, zsrc, z_ok);
         }
       }
+      if (++issue_gpos == spg) {
+        issue_gpos = 0;
+        ssrc += p.N;
+        if constexpr (HAS_ZP) zsrc += NW;
+      }
+      ++issue_i;
+      if (++issue_slot == kRing) issue_slot = 0;
     }
     cp_async_commit();
   };
@@ -200,17 +228,20 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   // ---- software pipeline ----
 #pragma unroll
-  for (int s = 0; s < kRing - 1; ++s) issue(s);
+  for (int s = 0; s < kRing - 1; ++s) issue();
 
+  int slot = 0, gpos = gpos0;
   for (int i = 0; i < nsteps; ++i) {
-    issue(i + kRing - 1);
+    issue();
     cp_async_wait<kRing - 1>();
     __syncwarp();
 
-    const int64_t ks = w_begin + i;
-    const uint32_t st = ring_u32 + (i % kRing) * L::kStage;
+    const uint32_t st = ring_u32 + slot * L::kStage;
+    if (++slot == kRing) slot = 0;
+    const bool new_group = i == 0 || gpos == 0;
+    if (++gpos == spg) gpos = 0;
 
-    if (i == 0 || ((ks * 16) % p.G) == 0) {
+    if (new_group) {
       // scale row: this lane's 8V columns start at column 8*V*gl of the tile
 #pragma unroll
       for (int v = 0; v < V; ++v) {
@@ -369,8 +400,7 @@ template <class DT, bool Z>
 Variant pick_vj(int V, int J) {
   if (J == 1) {
     if (V == 1) return {kernel_ptr<DT, 1, 1, Z>(), smem_bytes<1, 1, Z>()};
-    if (V == 2) return {kernel_ptr<DT, 2, 1, Z>(), smem_bytes<2, 1, Z>()};
-    return {kernel_ptr<DT, 4, 1, Z>(), smem_bytes<4, 1, Z>()};
+    return {kernel_ptr<DT, 2, 1, Z>(), smem_bytes<2, 1, Z>()};
   }
   if (J == 2) return {kernel_ptr<DT, 1, 2, Z>(), smem_bytes<1, 2, Z>()};
   return {kernel_ptr<DT, 1, 4, Z>(), smem_bytes<1, 4, Z>()};
@@ -391,23 +421,32 @@ bool decode_supported(const GemmArgs &g) {
 }
 
 void decode_make_plan(int64_t M, int64_t K, int64_t N, int has_zp, int num_sms, w4a16_plan_t *p) {
-  (void)has_zp;
-  int J = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
-  int V;
-  if (J > 1) {
-    V = 1;
-  } else {
-    const int64_t tiles2 = (N + 127) / 128;
-    V = tiles2 * 8 >= num_sms ? 2 : 1;
-  }
-  const int64_t n_tiles = (N + 64 * V - 1) / (64 * V);
-  const int64_t m_tiles = (M + 8 * J - 1) / (8 * J);
+  const int J = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
   const int64_t KS = K / 16;
-  const int64_t base = n_tiles * m_tiles;
-  int64_t C = base >= num_sms ? 1 : num_sms / base;
-  C = C < 1 ? 1 : (C > 8 ? 8 : C);
-  // every warp should get at least two k-steps
-  while (C > 1 && KS < C * kWarps * 2) --C;
+  const int64_t m_tiles = (M + 8 * J - 1) / (8 * J);
+  // Two CTAs of 8 warps fit on an SM (registers and shared memory): aim for one such wave.
+  const int64_t slots = 2 * int64_t(num_sms);
+  int bestV = 1, bestC = 1;
+  double best = -1.0;
+  for (int V = 2; V >= 1; --V) {
+    if (J > 1 && V != 1) continue;  // multi-tile rows: one word per lane keeps registers in check
+    const int64_t n_tiles = (N + 64 * V - 1) / (64 * V);
+    for (int C = 1; C <= 8; ++C) {
+      if (C > 1 && KS < int64_t(C) * kWarps) break;  // every warp keeps at least one k-step
+      const int64_t ctas = n_tiles * C * m_tiles;
+      const int64_t waves = (ctas + slots - 1) / slots;
+      double eff = double(ctas) / double(waves * slots);
+      if (V == 2) eff *= 1.08;  // wider loads and fewer column tiles: preferred at equal fill
+      if (eff > best + 1e-9) {
+        best = eff;
+        bestV = V;
+        bestC = C;
+      }
+    }
+  }
+  const int V = bestV;
+  const int64_t C = bestC;
+  const int64_t n_tiles = (N + 64 * V - 1) / (64 * V);
   const int64_t kc = (KS + C - 1) / C;
   p->path = W4A16_PATH_DECODE;
   p->words_per_lane = V;
@@ -430,7 +469,7 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   {
-    const int vi = V == 1 ? (J == 1 ? 0 : (J == 2 ? 3 : 4)) : (V == 2 ? 1 : 2);
+    const int vi = V == 1 ? (J == 1 ? 0 : (J == 2 ? 3 : 4)) : 1;
     std::lock_guard<std::mutex> lock(mu);
     bool &done = configured[dev & 63][g.dtype == W4A16_BF16][g.qzeros != nullptr][vi];
     if (!done) {
@@ -464,14 +503,17 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
   cfg.blockDim = dim3(kWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(var.smem);
   cfg.stream = g.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   int nattr = 0;
+  attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+  ++nattr;
   if (C > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(C);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    nattr = 1;
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = static_cast<unsigned>(C);
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
   }
   cfg.attrs = attr;
   cfg.numAttrs = nattr;

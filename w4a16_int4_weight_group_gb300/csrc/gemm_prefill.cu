@@ -1,23 +1,577 @@
-// Prefill path (tcgen05 / TMEM / TMA). Placeholder until the kernel lands: never selected.
+// Prefill path of the W4A16 product (large M): a TMA-fed tcgen05 GEMM that dequantises int4 weight
+// tiles into shared memory right before the tensor cores consume them.
+//
+// The pages' prefill kernel is a Triton tile loop (PR #51453 report, implementation breakdown: tile
+// BLOCK_M/N/K chosen at run time, BLOCK_K clamped to the group size; PR #40977 report, key source
+// snippets: fp32 accumulator, dequantise then multiply-add per K tile). On sm_103a this becomes:
+//
+//  * CTA tile 128 (rows of A) x 256 (output columns), K in blocks of 64. One CTA per tile, 10 warps:
+//      warp 0      TMA producer: A tile (128x64, 128-byte swizzle), packed weight tile (64 rows x 32
+//                  words), the one or two scale rows and zero-point rows the block needs;
+//      warp 1      TMEM allocator and the single MMA-issuing thread;
+//      warps 2..9  dequantisers, then the epilogue.
+//  * Dequantisation: each thread owns one packed word column (8 output columns) and 8 rows of the
+//    block; per word one LOP3 per output pair puts nibbles j and j+4 into the low mantissa bits of a
+//    packed fp16 (exponent of 1024, or 64 for high nibbles) or bf16 (exponent of 128) pair, an exact
+//    subtraction of (base + zp) yields q - zp, one packed multiply by the scale rounds once: exactly
+//    the value w4a16_dequant writes. The 16-byte result (columns n, n+4, n+1, n+5, ...) goes to the
+//    shared-memory B tile in the MN-major 128-byte-swizzled layout the tensor core reads; the epilogue
+//    undoes the column interleave.
+//  * MMA: tcgen05.mma.cta_group::1.kind::f16, M=128, N=256, K=16, fp32 accumulator in 256 TMEM
+//    columns; A K-major, B MN-major. tcgen05.commit frees the shared-memory stages.
+//  * Pipelines: 4 stages of (A, packed, scales, zeros) and 3 stages of dequantised B, each with
+//    full/empty mbarriers. Every wait is bounded (default 2 s, settable for tests): on expiry the CTA
+//    records an error word, stops, drains its own TMA copies and MMAs with a fixed bound, frees its
+//    TMEM and exits without writing output.
+//  * Epilogue: tcgen05.ld 32 columns at a time, + bias in fp32, one rounding to the dtype, 16-byte
+//    stores (PR #40977 report, key source snippets, test reference: bias before the cast).
+#include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched from the driver at run time
+
+#include <mutex>
+
+#include "common.cuh"
 #include "internal.h"
 
 namespace w4a16 {
+namespace {
 
-bool prefill_supported(const GemmArgs &) { return false; }
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int SA = 4;  // stages of A / packed weights / scales / zeros
+constexpr int SB = 3;  // stages of dequantised weights
+constexpr int kDequantWarps = 8;
+constexpr int kThreads = 32 * (2 + kDequantWarps);
+constexpr uint32_t kTmemCols = 256;
 
-void prefill_make_plan(int64_t, int64_t, int64_t, int, int, w4a16_plan_t *p) {
+constexpr int kABytes = BM * BK * 2;        // 16 KB
+constexpr int kPBytes = BK * (BN / 8) * 4;  // 8 KB
+constexpr int kSBytes = 2 * BN * 2;         // up to two scale rows
+constexpr int kZBytes = 2 * (BN / 8) * 4;   // up to two zero-point rows
+constexpr int kBBytes = BK * BN * 2;        // 32 KB
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + SA * kABytes;
+constexpr int kOffP = kOffB + SB * kBBytes;
+constexpr int kOffS = kOffP + SA * kPBytes;
+constexpr int kOffZ = kOffS + SA * kSBytes;
+constexpr int kOffBar = kOffZ + SA * kZBytes;
+constexpr int kNumBars = 2 * SA + 2 * SB + 1;
+constexpr int kOffSlot = kOffBar + kNumBars * 8;
+constexpr int kOffFlag = kOffSlot + 4;
+constexpr int kSmemUsed = kOffFlag + 4;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 bytes
+static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kDrainWaitNs = 1000000000ull;    // 1 s, for draining own copies after an abort
+
+__device__ unsigned int g_prefill_error;
+__device__ unsigned long long g_wait_limit_ns;
+
+// ---------------------------------------------------------------------------------------------
+// PTX wrappers: mbarrier, TMA, tcgen05
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start >> 4 in bits 0-13, leading byte offset >> 4 in
+// 16-29, stride byte offset >> 4 in 32-45, the fixed 0b001 in 46-48, swizzle mode in 61-63
+// (2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
+         (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Bounded wait on an mbarrier phase. Returns false if this CTA is aborting (flag set here on timeout).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                           uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      *abort_flag = 1u;
+      atomicOr(&g_prefill_error, 1u);
+      return false;
+    }
+  }
+}
+// Drain wait after an abort: ignores the abort flag, fixed bound.
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kDrainWaitNs) {
+      atomicOr(&g_prefill_error, 2u);
+      return;
+    }
+  }
+}
+
+struct PrefillParams {
+  const uint16_t *bias;
+  uint16_t *out;
+  int64_t M, K, N;
+  int G;
+  int zp_bias;
+  int nk;     // K blocks of 64
+  int srows;  // scale / zero-point rows loaded per K block (2 when a block can span two groups)
+};
+
+template <bool BF>
+__device__ __forceinline__ void magic4(uint32_t w, uint32_t (&h)[4]) {
+  // h[i] = packed (base + nibble i, base + nibble i+4) with an exact integer in the low mantissa bits
+  if constexpr (BF) {
+    h[0] = and_or(w, 0x000F000Fu, 0x43004300u);
+    h[1] = and_or(w >> 4, 0x000F000Fu, 0x43004300u);
+    h[2] = and_or(w >> 8, 0x000F000Fu, 0x43004300u);
+    h[3] = and_or(w >> 12, 0x000F000Fu, 0x43004300u);
+  } else {
+    const uint32_t w8 = w >> 8;
+    h[0] = and_or(w, 0x000F000Fu, 0x64006400u);   // 1024 + q
+    h[1] = and_or(w, 0x00F000F0u, 0x54005400u);   // 64 + q (high nibble of a byte, ulp 1/16)
+    h[2] = and_or(w8, 0x000F000Fu, 0x64006400u);
+    h[3] = and_or(w8, 0x00F000F0u, 0x54005400u);
+  }
+}
+
+template <class DT, bool HAS_ZP>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmP,
+                   const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ,
+                   const PrefillParams p) {
+  constexpr bool BF = DT::kBF16;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+  uint8_t *base_ptr = smem_raw + (base - raw_u32);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t m0 = int64_t(blockIdx.x) * BM;
+  const int64_t n0 = int64_t(blockIdx.y) * BN;
+
+  const uint32_t bar0 = base + kOffBar;
+  auto full_a = [&](int s) { return bar0 + 8u * s; };
+  auto empty_a = [&](int s) { return bar0 + 8u * (SA + s); };
+  auto full_b = [&](int s) { return bar0 + 8u * (2 * SA + s); };
+  auto empty_b = [&](int s) { return bar0 + 8u * (2 * SA + SB + s); };
+  const uint32_t accum_full = bar0 + 8u * (2 * SA + 2 * SB);
+  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(base_ptr + kOffFlag);
+  const uint32_t slot = base + kOffSlot;
+
+  const unsigned long long lim = g_wait_limit_ns;
+  const uint64_t limit_ns = lim ? lim : kDefaultWaitNs;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(full_a(s), 1);
+      mbar_init(empty_a(s), kDequantWarps + 1);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(full_b(s), kDequantWarps);
+      mbar_init(empty_b(s), 1);
+    }
+    mbar_init(accum_full, 1);
+    *abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(base_ptr + kOffSlot);
+
+  const int nk = p.nk;
+  const int srows = p.srows;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t tx = kABytes + kPBytes + srows * (BN * 2) + (HAS_ZP ? srows * (BN / 8) * 4 : 0);
+      int issued = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % SA;
+        const uint32_t ph = (kb / SA) & 1;
+        if (!wait_phase(empty_a(s), ph ^ 1u, abort_flag, limit_ns)) break;
+        mbar_arrive_expect_tx(full_a(s), tx);
+        const int k0 = kb * BK;
+        const int grow = static_cast<int>(int64_t(k0) / p.G);
+        tma_load_2d(base + kOffA + s * kABytes, &tmA, k0, static_cast<int>(m0), full_a(s));
+        tma_load_2d(base + kOffP + s * kPBytes, &tmP, static_cast<int>(n0 / 8), k0, full_a(s));
+        tma_load_2d(base + kOffS + s * kSBytes, &tmS, static_cast<int>(n0), grow, full_a(s));
+        if constexpr (HAS_ZP) tma_load_2d(base + kOffZ + s * kZBytes, &tmZ, static_cast<int>(n0 / 8), grow, full_a(s));
+        issued = kb + 1;
+      }
+      if (*abort_flag) {
+        // let this CTA's own copies land before its shared memory is released
+        for (int kb = issued - 1; kb >= 0 && kb >= issued - SA; --kb) drain_phase(full_a(kb % SA), (kb / SA) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = (1u << 4)                         // D: fp32
+                             | ((BF ? 1u : 0u) << 7)           // A: f16 / bf16
+                             | ((BF ? 1u : 0u) << 10)          // B: f16 / bf16
+                             | (0u << 15)                      // A K-major
+                             | (1u << 16)                      // B MN-major
+                             | (uint32_t(BN >> 3) << 17)       // N
+                             | (uint32_t(BM >> 4) << 24);      // M
+      bool ok = true;
+      for (int kb = 0; kb < nk && ok; ++kb) {
+        const int sa = kb % SA, sb = kb % SB;
+        ok = wait_phase(full_a(sa), (kb / SA) & 1, abort_flag, limit_ns) &&
+             wait_phase(full_b(sb), (kb / SB) & 1, abort_flag, limit_ns);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a_base = base + kOffA + sa * kABytes;
+        const uint32_t b_base = base + kOffB + sb * kBBytes;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; a K step of 16 is 32 bytes.
+          const uint64_t ad = smem_desc(a_base + 32u * kk, 16u, 1024u);
+          // B: MN-major, 128-byte swizzle atoms of 64 columns x 8 rows; atoms along N 1024 B apart
+          // (leading), 8-row K groups 4096 B apart (stride); a K step of 16 is two groups.
+          const uint64_t bd = smem_desc(b_base + 8192u * kk, 1024u, 4096u);
+          umma_f16(tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+        }
+        umma_commit(empty_a(sa));
+        umma_commit(empty_b(sb));
+      }
+      umma_commit(accum_full);
+      if (!ok) drain_phase(accum_full, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ dequantisers
+    const int dw = warp - 2;  // 0..7
+    const int c = lane;       // packed word column of the tile (8 output columns)
+    bool ok = true;
+    uint32_t zsub[2][4], spair[2][4];
+    if constexpr (!HAS_ZP) {
+      const uint32_t zb = static_cast<uint32_t>(p.zp_bias);
+      // base + zp for nibbles j (low half of a byte) and j+1 (high half; fp16 uses base 64 there)
+      const uint32_t lo = BF ? (0x4300u | zb) : (0x6400u | zb);
+      const uint32_t hi = BF ? (0x4300u | zb) : (0x5400u | (zb << 4));
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        zsub[g][0] = zsub[g][2] = lo | (lo << 16);
+        zsub[g][1] = zsub[g][3] = hi | (hi << 16);
+      }
+    }
+    for (int kb = 0; kb < nk; ++kb) {
+      const int sa = kb % SA, sb = kb % SB;
+      ok = wait_phase(full_a(sa), (kb / SA) & 1, abort_flag, limit_ns) &&
+           wait_phase(empty_b(sb), ((kb / SB) & 1) ^ 1u, abort_flag, limit_ns);
+      ok = __all_sync(0xffffffffu, ok);  // the warp leaves the loop together
+      if (!ok) break;
+      const uint32_t P = base + kOffP + sa * kPBytes;
+      const uint32_t S = base + kOffS + sa * kSBytes;
+      const uint32_t Z = base + kOffZ + sa * kZBytes;
+      const uint32_t B = base + kOffB + sb * kBBytes;
+      const int64_t k0 = int64_t(kb) * BK;
+      const int64_t g0 = k0 / p.G;
+#pragma unroll
+      for (int gr = 0; gr < 2; ++gr) {
+        if (gr < srows) {
+          uint32_t s01, s23, s45, s67;
+          lds128(S + gr * (BN * 2) + c * 16, s01, s23, s45, s67);
+          spair[gr][0] = prmt(s01, s45, 0x5410);  // (s0, s4)
+          spair[gr][1] = prmt(s01, s45, 0x7632);  // (s1, s5)
+          spair[gr][2] = prmt(s23, s67, 0x5410);  // (s2, s6)
+          spair[gr][3] = prmt(s23, s67, 0x7632);  // (s3, s7)
+          if constexpr (HAS_ZP) magic4<BF>(lds32(Z + gr * (BN / 2) + c * 4), zsub[gr]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < BK / kDequantWarps; ++i) {
+        const int r = dw + kDequantWarps * i;
+        int gr = srows == 2 ? static_cast<int>((k0 + r) / p.G - g0) : 0;
+        gr = gr > 1 ? 1 : gr;
+        const uint32_t wq = lds32(P + r * (BN / 2) + c * 4);
+        uint32_t h[4];
+        magic4<BF>(wq, h);
+        uint32_t x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t zz = gr ? zsub[1][j] : zsub[0][j];
+          const uint32_t ss = gr ? spair[1][j] : spair[0][j];
+          x[j] = mul2_rn<BF>(sub2_rn<BF>(h[j], zz), ss);
+        }
+        // MN-major, 128-byte swizzle: 8-row K groups 4096 B apart, 64-column atoms 1024 B apart,
+        // row r%8 at 128 B, 16-byte chunk (c%8) XOR (r%8).
+        const uint32_t off = (r >> 3) * 4096u + (c >> 3) * 1024u + (r & 7) * 128u + ((((c & 7) ^ (r & 7))) << 4);
+        sts128(B + off, x[0], x[1], x[2], x[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(full_b(sb));
+        mbar_arrive(empty_a(sa));
+      }
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (ok) ok = wait_phase(accum_full, 0, abort_flag, limit_ns);
+    ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
+    tc_fence_after();
+    const int q = warp & 3;                // TMEM lane quarter this warp may read
+    const int row = 32 * q + lane;
+    const int half = dw >> 2;              // columns [128*half, 128*half + 128)
+    const int64_t m = m0 + row;
+    const bool row_ok = m < p.M;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      const int col0 = half * 128 + ch * 32;
+      uint32_t r[32];
+      if (ok) {
+        tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(col0), r);
+        tmem_wait_ld();
+      }
+      if (ok && row_ok) {
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) {
+          const int64_t n = n0 + col0 + 8 * g8;
+          if (n < p.N) {
+            // accumulator columns hold outputs n+0, n+4, n+1, n+5, n+2, n+6, n+3, n+7
+            float v[8];
+            v[0] = __uint_as_float(r[8 * g8 + 0]);
+            v[4] = __uint_as_float(r[8 * g8 + 1]);
+            v[1] = __uint_as_float(r[8 * g8 + 2]);
+            v[5] = __uint_as_float(r[8 * g8 + 3]);
+            v[2] = __uint_as_float(r[8 * g8 + 4]);
+            v[6] = __uint_as_float(r[8 * g8 + 5]);
+            v[3] = __uint_as_float(r[8 * g8 + 6]);
+            v[7] = __uint_as_float(r[8 * g8 + 7]);
+            if (p.bias) {
+              const uint4 bv = *reinterpret_cast<const uint4 *>(p.bias + n);
+              const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                v[2 * e] += bits_to_float(static_cast<uint16_t>(bw[e] & 0xFFFFu), BF);
+                v[2 * e + 1] += bits_to_float(static_cast<uint16_t>(bw[e] >> 16), BF);
+              }
+            }
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if constexpr (BF) {
+                const __nv_bfloat162 t = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                o[e] = *reinterpret_cast<const uint32_t *>(&t);
+              } else {
+                const __half2 t = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
+                o[e] = *reinterpret_cast<const uint32_t *>(&t);
+              }
+            }
+            *reinterpret_cast<uint4 *>(p.out + m * p.N + n) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------------
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encoder() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+  });
+  return fn;
+}
+
+bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return encoder()(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                          const PrefillParams);
+
+KernelFn pick(int dtype, bool zp) {
+  if (dtype == W4A16_BF16) return zp ? prefill_kernel<BF16, true> : prefill_kernel<BF16, false>;
+  return zp ? prefill_kernel<F16, true> : prefill_kernel<F16, false>;
+}
+
+}  // namespace
+
+bool prefill_supported(const GemmArgs &g) {
+  return g.N % 32 == 0 && g.K % 8 == 0 && aligned16(g.a) && aligned16(g.b_q) && aligned16(g.scales) &&
+         aligned16(g.out) && (g.qzeros == nullptr || aligned16(g.qzeros)) && (g.bias == nullptr || aligned16(g.bias)) &&
+         (g.N + BN - 1) / BN <= 65535 && encoder() != nullptr;
+}
+
+void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, w4a16_plan_t *p) {
+  (void)K;
+  (void)group_size;
+  (void)num_sms;
   p->path = W4A16_PATH_PREFILL;
+  p->words_per_lane = 1;
+  p->m_tile = BM;
+  p->n_tile = BN;
+  p->k_split = 1;
+  p->warps = kThreads / 32;
+  p->grid = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  p->smem_bytes = kSmemBytes;
+  p->reserved = 0;
 }
 
-cudaError_t launch_gemm_prefill(const GemmArgs &, const w4a16_plan_t &) {
-  return cudaErrorNotSupported;
-}
+cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &) {
+  const bool zp = g.qzeros != nullptr;
+  const int64_t NW = g.N / 8, ng = g.K / g.group_size;
+  const int srows = g.group_size < BK ? 2 : 1;
+  CUtensorMap tA, tP, tS, tZ;
+  if (!encode_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.a, g.K, g.M, g.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tP, CU_TENSOR_MAP_DATA_TYPE_INT32, g.b_q, NW, g.K, NW * 4, BN / 8, BK, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_2d(&tS, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.scales, g.N, ng, g.N * 2, BN, srows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  if (zp) {
+    if (!encode_2d(&tZ, CU_TENSOR_MAP_DATA_TYPE_INT32, g.qzeros, NW, ng, NW * 4, BN / 8, srows,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
+    tZ = tP;  // unused
+  }
+  const KernelFn fn = pick(g.dtype, zp);
+  {
+    static std::mutex mu;
+    static bool configured[64][2][2] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][zp];
+    if (!done) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess) return e;
+      done = true;
+    }
+  }
+  PrefillParams prm;
+  prm.bias = static_cast<const uint16_t *>(g.bias);
+  prm.out = static_cast<uint16_t *>(g.out);
+  prm.M = g.M;
+  prm.K = g.K;
+  prm.N = g.N;
+  prm.G = g.group_size;
+  prm.zp_bias = g.zp_bias;
+  prm.nk = static_cast<int>((g.K + BK - 1) / BK);
+  prm.srows = srows;
 
-cudaError_t prefill_take_device_error(uint32_t *err) {
-  *err = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((g.M + BM - 1) / BM), static_cast<unsigned>((g.N + BN - 1) / BN), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = g.stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tA, tP, tS, tZ, prm);
+  if (e != cudaSuccess) return e;
+  note_launch();
   return cudaSuccess;
 }
 
-cudaError_t prefill_set_wait_limit_ns(uint64_t) { return cudaSuccess; }
+cudaError_t prefill_take_device_error(uint32_t *err) {
+  uint32_t v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_prefill_error, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v) e = cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(zero));
+  *err = v;
+  return e;
+}
+
+cudaError_t prefill_set_wait_limit_ns(uint64_t ns) {
+  const unsigned long long v = ns;
+  return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof(v));
+}
 
 }  // namespace w4a16
