@@ -114,9 +114,9 @@ def test_dispatcher_decode_for_small_m_and_split_k(w):
     # a narrow layer gets split along K across a cluster
     p = w.w4a16_plan(1, 2112, 1152, 32, 1, False, 152)
     assert p["k_split"] > 1
-    # a wide one needs at most a pair of K splits to fill two CTAs per SM
+    # a wide one is split only as far as needed to fill two CTAs per SM
     p = w.w4a16_plan(1, 2560, 19456, 128, 0, True, 152)
-    assert p["k_split"] <= 2 and 152 <= p["grid"] <= 304
+    assert p["k_split"] <= 4 and 152 <= p["grid"] <= 304
     # and the choice follows the device: half the SMs, half the CTAs
     assert w.w4a16_plan(1, 2560, 19456, 128, 0, True, 76)["grid"] <= 152
 

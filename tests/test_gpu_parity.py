@@ -193,3 +193,27 @@ def test_decode_4b_workload_sampled_columns(w, args):
     out = run(w, c)
     cols = sample_cols(N, np.random.default_rng(seed))
     check_against_oracle(c, out, cols=cols, label="sampled")
+
+
+@pytest.mark.parametrize("args", list(synth.config_cases("prefill")), ids=_config_ids("prefill"))
+def test_prefill_workload_sampled(w, args):
+    """The prefill workload at full size, in the launch configuration the benchmark times."""
+    M, K, N, G, dt, asym, bias, lo, hi, seed = args
+    c = synth.make_case(M, K, N, G, dt, asym=asym, bias=bias, seed=seed, scale_lo=lo, scale_hi=hi)
+    assert w.w4a16_plan(M, K, N, G, 1 if dt == "bf16" else 0, asym, 0)["path_name"] == "prefill"
+    out = run(w, c)
+    rng = np.random.default_rng(seed)
+    rows = sorted({0, 1, 127, 128, M // 2, M - 1} | set(rng.integers(0, M, size=4).tolist()))
+    cols = sample_cols(N, rng, k=512)
+    check_against_oracle(c, out, rows=rows, cols=cols, label="prefill sampled")
+
+
+@pytest.mark.parametrize("M,K,N,G", [(1024, 5120, 7168, 128), (256, 17408, 512, 17408)])
+def test_sweep_shapes_sampled(w, M, K, N, G):
+    """27B-class layer shapes of the M sweep, per-group and per-channel scales."""
+    for dt, asym in (("f16", False), ("bf16", True)):
+        c = synth.make_case(M, K, N, G, dt, asym=asym, seed=M + G)
+        out = run(w, c)
+        rng = np.random.default_rng(M)
+        rows = sorted({0, M - 1} | set(rng.integers(0, M, size=4).tolist()))
+        check_against_oracle(c, out, rows=rows, cols=sample_cols(N, rng, k=256), label=f"{dt} {asym}")

@@ -89,15 +89,15 @@ int forced_path() {
 // M at and above which the tcgen05 path is preferred when it applies.
 constexpr int64_t kPrefillMinM = 65;
 
-void choose_plan(const GemmArgs &g, int num_sms, w4a16_plan_t *p) {
+// `tma` tells whether the driver's tensor-map encoder is available (the TMA-fed paths need it).
+void choose_plan(const GemmArgs &g, int num_sms, bool tma, w4a16_plan_t *p) {
   std::memset(p, 0, sizeof(*p));
   if (g.M == 0) {
     p->path = W4A16_PATH_NONE;
     return;
   }
-  // the decode grid indexes row tiles of up to 32 rows in a dimension of at most 65535
-  const bool dec = decode_supported(g) && (g.M + 31) / 32 <= 65535;
-  const bool pre = prefill_supported(g);
+  const bool dec = tma && decode_supported(g);
+  const bool pre = tma && prefill_supported(g);
   const int force = forced_path();
   int path;
   if (force == W4A16_PATH_GENERIC || (!dec && !pre)) {
@@ -114,7 +114,7 @@ void choose_plan(const GemmArgs &g, int num_sms, w4a16_plan_t *p) {
     path = W4A16_PATH_GENERIC;
   }
   if (path == W4A16_PATH_DECODE) {
-    decode_make_plan(g.M, g.K, g.N, g.qzeros != nullptr, num_sms, p);
+    decode_make_plan(g.M, g.K, g.N, g.group_size, num_sms, p);
   } else if (path == W4A16_PATH_PREFILL) {
     prefill_make_plan(g.M, g.K, g.N, g.group_size, num_sms, p);
   } else {
@@ -130,6 +130,41 @@ void choose_plan(const GemmArgs &g, int num_sms, w4a16_plan_t *p) {
 }  // namespace
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeFn tma_encoder() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+  });
+  return fn;
+}
+}  // namespace
+
+bool tma_available() { return tma_encoder() != nullptr; }
+
+bool tma_encode_2d(CUtensorMap *map, int elem_bytes, const void *ptr, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle_128b) {
+  const EncodeFn enc = tma_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  return enc(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle_128b ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t current_device_info(DeviceInfo *info) {
   static std::mutex mu;
@@ -270,7 +305,7 @@ w4a16_status w4a16_gemm(const void *a, const int32_t *b_q, const void *scales, c
   cudaError_t e = current_device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "device query");
   w4a16_plan_t plan;
-  choose_plan(g, dev.num_sms, &plan);
+  choose_plan(g, dev.num_sms, tma_available(), &plan);
   switch (plan.path) {
     case W4A16_PATH_DECODE: e = launch_gemm_decode(g, plan); break;
     case W4A16_PATH_PREFILL: e = launch_gemm_prefill(g, plan); break;
@@ -298,7 +333,7 @@ w4a16_status w4a16_plan(int64_t m, int64_t k, int64_t n, int group_size, int dty
       (reinterpret_cast<uintptr_t>(kAlignedWord) + 15) & ~uintptr_t(15));
   GemmArgs g{p16, static_cast<const int32_t *>(p16), p16, has_zp ? static_cast<const int32_t *>(p16) : nullptr,
              group_size, 8, nullptr, nullptr, m, k, n, dtype, nullptr};
-  choose_plan(g, num_sms, plan);
+  choose_plan(g, num_sms, /*tma=*/true, plan);  // a host-only query: assume a GPU driver
   return ok();
 }
 
@@ -311,15 +346,18 @@ int w4a16_debug_selected_path(int64_t m, int64_t k, int64_t n, int group_size) {
 w4a16_status w4a16_get_device_error(void) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "synchronise");
-  uint32_t err = 0;
+  uint32_t err = 0, err2 = 0;
   e = prefill_take_device_error(&err);
+  if (e == cudaSuccess) e = decode_take_device_error(&err2);
   if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  err |= err2;
   if (err) return fail(W4A16_ERR_TIMEOUT, "a bounded device-side wait gave up (code 0x%x)", err);
   return ok();
 }
 
 w4a16_status w4a16_debug_set_wait_limit_ns(uint64_t ns) {
-  const cudaError_t e = prefill_set_wait_limit_ns(ns);
+  cudaError_t e = prefill_set_wait_limit_ns(ns);
+  if (e == cudaSuccess) e = decode_set_wait_limit_ns(ns);
   if (e != cudaSuccess) return cuda_fail(e, "set wait limit");
   return ok();
 }

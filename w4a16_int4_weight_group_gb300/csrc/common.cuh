@@ -152,4 +152,91 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
   return v;
 }
 
+
+// ---------------------------------------------------------------------------------------------
+// mbarrier, TMA (cp.async.bulk.tensor) and bounded waits
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Returns true once the phase with the given parity has completed. The thread may be suspended for
+// up to `hint_ns` inside the instruction while it waits, which keeps polling off the issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns = 1000u) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// 2-D tiled TMA load into shared memory, completion counted on an mbarrier (bytes).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tensor_map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Bounded wait on an mbarrier phase. On expiry it sets *abort_flag (shared) and ORs `code` into the
+// kernel's device error word; it also returns false early once another thread has set the flag.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                           uint64_t limit_ns, unsigned int *error_word) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      *abort_flag = 1u;
+      atomicOr(error_word, 1u);
+      return false;
+    }
+  }
+}
+// Wait used after an abort to let this CTA's own copies or MMAs land: ignores the abort flag and
+// has its own fixed bound.
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, unsigned int *error_word,
+                                            uint64_t limit_ns = 1000000000ull) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > limit_ns) {
+      atomicOr(error_word, 2u);
+      return;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// ldmatrix: four 8x8 matrices of 16-bit elements; lanes 8i..8i+7 give the row addresses of matrix i.
+// Without .trans lane t receives (row t/4, columns 2(t%4), 2(t%4)+1); with .trans it receives
+// (rows 2(t%4), 2(t%4)+1 of column t/4).
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
 }  // namespace w4a16

@@ -1,35 +1,35 @@
-// Decode / skinny path of the W4A16 product (small M): a split-K GEMM that streams the packed
-// weights once from HBM, dequantises them in registers and multiplies on the tensor cores.
+// Decode / skinny path of the W4A16 product (M <= 16): a split-K GEMM that streams the packed
+// weights once from HBM through TMA, dequantises them in registers and multiplies on the tensor cores.
 //
-// Where the ideas come from (PR #40977 report, implementation breakdown item 3 - a split-K skinny
-// decode kernel with magic-number int4 -> half dequantisation and a cross-lane reduction; PR #51453
-// report, review highlights - split-K requested because small-M decode leaves the GPU idle), and what
-// this kernel does on sm_103a instead:
+// Where the ideas come from: the PR #40977 report (implementation breakdown item 3) describes a
+// split-K skinny decode kernel with magic-number int4 -> half dequantisation and a cross-lane
+// reduction; the PR #51453 report (review highlights) asks for split-K because small-M decode leaves
+// the GPU idle. What this kernel does on sm_103a:
 //
-//  * Work split. A CTA owns 64*V output columns (V packed words per lane per row) and 8*J rows of A.
-//    Its W warps split the CTA's K range into contiguous pieces; C CTAs of one thread-block cluster
-//    split K further. Partial sums are added in shared memory (warps) and through distributed shared
-//    memory (cluster ranks) in a fixed order, so results are deterministic and no global scratch
-//    memory is needed.
-//  * Streaming. Each warp owns a ring of R shared-memory stages. One stage is one k-step of 16 rows:
-//    16 x 32V bytes of packed weights, the matching 16 columns of A (rows past M zero-filled), and at
-//    group starts the scale row (and zero-point words). All of it arrives by 16-byte cp.async
-//    (coalesced, L2-only), R-1 stages ahead of the math, so no registers hold data in flight.
-//    The weight stage layout is XOR-swizzled so that the fragment reads below are bank-conflict free.
-//  * Dequantisation (magic numbers, one rounding). For two rows k, k+1 of one word column, one byte
-//    permute interleaves their nibbles so that a single LOP3 places nibble j of both rows into the
-//    low mantissa bits of two fp16 (exponent of 1024, or 64 for the high nibble of a byte) or bf16
-//    (exponent of 128) values: the packed pair is then exactly (base+q_k, base+q_k+1). Subtracting
-//    (base+zp) is exact and gives the integers q - zp; one packed multiply by the scale rounds once,
-//    giving exactly RNE((q - zp) * s), the values w4a16_dequant writes.
-//  * Multiply. mma.sync m16n8k16 with the weights as the 16-row operand (16 output columns) and the
-//    activations as the 8-column operand (8 rows of A): the pages' M <= 8 decode batch fills the
-//    n=8 side. The k order inside an MMA is a free permutation; it is chosen so that each lane's
-//    k values are 4 consecutive rows (one 8-byte activation load) and each register pair is a row
-//    pair (k, k+1) of one output column.
-//  * Epilogue. Bias is added in fp32, the sum is rounded once to the activation dtype
-//    (PR #40977 report, key source snippets, test reference).
-#include <algorithm>
+//  * Work split. A CTA owns 256 output columns and a contiguous range of K blocks (64 rows each);
+//    the C CTAs of one thread-block cluster split K. Nine warps: one TMA producer and eight
+//    consumers, consumer w owning columns [32w, 32w+32) of the tile for the whole K range, so no
+//    reduction is needed inside the CTA. Cluster ranks add their partial tiles through distributed
+//    shared memory in a fixed order: deterministic, and no global scratch memory.
+//  * Streaming. Per K block one TMA box of packed weights (64 rows x 128 bytes, 128-byte swizzle),
+//    the activation rows (8 or 16 x 64, zero-filled past M), and the scale and zero-point rows of the
+//    block's one or two groups land in an 8-deep ring of shared-memory stages guarded by full/empty
+//    mbarriers; the producer runs up to 8 blocks ahead, so 64 KB per CTA are in flight.
+//  * Fragments. Viewing a packed row as 16-bit elements (4 nibbles = 4 consecutive columns each),
+//    ldmatrix.trans delivers to lane (g, t) the element of rows 2t and 2t+1 for column quad g: the
+//    two rows of a k pair side by side, which is what a 16-bit MMA register holds. The 128-byte
+//    swizzle makes the eight row addresses of each 8x8 matrix hit distinct banks.
+//  * Dequantisation (magic numbers, one rounding). One LOP3 places the nibble of column j of both
+//    rows into the low mantissa bits of a packed fp16 pair with exponent of 1024 (64 for the high
+//    nibble of a byte) or a bf16 pair with exponent of 128: the pair is exactly (base+q_k, base+q_k+1).
+//    Subtracting (base+zp) is exact; one packed multiply by the scale rounds once, giving exactly
+//    RNE((q - zp) * s), the values w4a16_dequant writes.
+//  * Multiply. mma.sync m16n8k16 with 16 output columns as the MMA rows and up to 8 rows of A as the
+//    MMA columns (the M <= 8 decode batch fills the n=8 side; M <= 16 takes two MMAs).
+//  * Epilogue. Bias is added in fp32 and the sum rounded once to the activation dtype (PR #40977
+//    report, key source snippets, test reference).
+//  * Every mbarrier wait is bounded: on expiry the CTA records an error word, its warps leave the
+//    loop, the producer drains its own copies, and the CTA still takes part in the cluster barriers.
 #include <mutex>
 
 #include "common.cuh"
@@ -38,339 +38,291 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kRing = 6;    // stages per warp
+constexpr int kConsumers = 8;                  // one per 32-column block
+constexpr int kThreads = 32 * (kConsumers + 1);
+constexpr int BN = 256;                        // output columns per CTA
+constexpr int BK = 64;                         // rows of K per stage
+constexpr int kStages = 8;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
-__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
-constexpr int kWarps = 8;   // warps per CTA
+__device__ unsigned int g_decode_error;
+__device__ unsigned long long g_decode_wait_limit_ns;
 
-template <int V, int J, bool HAS_ZP>
-struct DecodeLayout {
-  static constexpr int kWN = 64 * V;                   // output columns per CTA
-  static constexpr int kMT = 8 * J;                    // rows of A per CTA
-  static constexpr int kWBytes = 16 * 32 * V;          // 16 rows x 8V words
-  static constexpr int kABytes = kMT * 32;             // kMT rows x 16 halves
-  static constexpr int kSBytes = kWN * 2;              // one scale row
-  static constexpr int kZBytes = HAS_ZP ? kWN / 2 : 0; // one zero-point row (8V words)
-  static constexpr int kA = kWBytes;
-  static constexpr int kS = kA + kABytes;
-  static constexpr int kZ = kS + kSBytes;
-  static constexpr int kStage = kZ + kZBytes;
-  static constexpr int kWarpRing = kStage * kRing;
-  static constexpr int kRingBytes = kWarpRing * kWarps;
-  static constexpr int kRedBytes = kWarps * kMT * kWN * 4;
-  static constexpr int kSmem = kRingBytes > kRedBytes ? kRingBytes : kRedBytes;
-  static_assert(kStage % 16 == 0, "stage must keep 16-byte alignment");
+template <int J>
+struct Layout {
+  static constexpr int kP = BK * BN / 2;        // 8 KB packed weights
+  static constexpr int kA = 8 * J * BK * 2;     // 1 KB per 8 rows of A
+  static constexpr int kS = 2 * BN * 2;         // up to two scale rows
+  static constexpr int kZ = 2 * (BN / 8) * 4;   // up to two zero-point rows
+  static constexpr int kOffP = 0;
+  static constexpr int kOffA = kOffP + kStages * kP;
+  static constexpr int kOffS = kOffA + kStages * kA;
+  static constexpr int kOffZ = kOffS + kStages * kS;
+  static constexpr int kOffBar = kOffZ + kStages * kZ;
+  static constexpr int kOffFlag = kOffBar + 2 * kStages * 8;
+  static constexpr int kUsed = kOffFlag + 16;
+  static constexpr int kSmem = kUsed + 1024;    // slack to align the base to 1024 bytes
+  static constexpr int kRedBytes = 8 * J * BN * 4;
+  static_assert(kRedBytes <= kStages * kP, "reduction buffer aliases the weight stages");
+  static_assert(kOffA % 1024 == 0 && kA % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
 
-// Byte offset of 16-byte chunk c of weight row `row` (0..15) inside a stage. Rows are 32V bytes;
-// 4/V rows share a 128-byte line, and chunk positions are XOR-swizzled by bits 2..3 of the row.
-template <int V>
-__device__ __forceinline__ uint32_t w_chunk_offset(int row, int c) {
-  constexpr int kRowsPerLine = 4 / V;
-  const int line = row / kRowsPerLine;
-  const int pos = (((row % kRowsPerLine) * (2 * V)) + c) ^ (2 * ((row >> 2) & 3));
-  return static_cast<uint32_t>(line * 128 + pos * 16);
-}
-
 struct DecodeParams {
-  const uint16_t *a;
-  const int32_t *b_q;
-  const uint16_t *scales;
-  const int32_t *qzeros;
   const uint16_t *bias;
   uint16_t *out;
   int64_t M, K, N;
   int G;
   int zp_bias;
-  int k_split;        // C: CTAs per cluster along K
-  int ksteps_per_cta; // k-steps (16 rows) per cluster rank
+  int k_split;      // C: CTAs per cluster along K
+  int kb_per_cta;   // K blocks per cluster rank
+  int kb_total;     // K blocks of the problem
+  int spg;          // K blocks per scale group (>= 1)
 };
 
-template <class DT, int V, int J, bool HAS_ZP>
-__global__ void __launch_bounds__(kWarps * 32, 2)
-    decode_kernel(const DecodeParams p) {
-  using L = DecodeLayout<V, J, HAS_ZP>;
+// base + zp for nibble j of a column quad: fp16 uses 1024 (even j) and 64 (odd j, high nibble of a
+// byte, mantissa ulp 1/16); bf16 uses 128. Packed twice (both rows of a k pair).
+template <bool BF>
+__device__ __forceinline__ uint32_t zsub_of(int j, uint32_t zp) {
+  uint32_t h;
+  if constexpr (BF) h = 0x4300u | zp;
+  else h = (j & 1) ? (0x5400u | (zp << 4)) : (0x6400u | zp);
+  return h | (h << 16);
+}
+
+// Packed (base + q) pairs of the four columns of a quad from one ldmatrix.trans register
+// (low half: row k, high half: row k+1, four nibbles each).
+template <bool BF>
+__device__ __forceinline__ void magic_quad(uint32_t w, uint32_t (&h)[4]) {
+  if constexpr (BF) {
+    h[0] = and_or(w, 0x000F000Fu, 0x43004300u);
+    h[1] = and_or(w >> 4, 0x000F000Fu, 0x43004300u);
+    h[2] = and_or(w >> 8, 0x000F000Fu, 0x43004300u);
+    h[3] = and_or(w >> 12, 0x000F000Fu, 0x43004300u);
+  } else {
+    const uint32_t w8 = w >> 8;
+    h[0] = and_or(w, 0x000F000Fu, 0x64006400u);
+    h[1] = and_or(w, 0x00F000F0u, 0x54005400u);
+    h[2] = and_or(w8, 0x000F000Fu, 0x64006400u);
+    h[3] = and_or(w8, 0x00F000F0u, 0x54005400u);
+  }
+}
+
+template <class DT, int J, bool HAS_ZP, bool TWO_GROUPS>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmP,
+                  const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ,
+                  const DecodeParams p) {
+  using L = Layout<J>;
   using T = typename DT::T;
   constexpr bool BF = DT::kBF16;
-  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kSRows = TWO_GROUPS ? 2 : 1;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+  uint8_t *base_ptr = smem_raw + (base - raw_u32);
 
-  const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int gl = lane >> 2;   // "groupID" of the MMA fragment layouts
-  const int tig = lane & 3;   // thread in group
+  const int lane = threadIdx.x & 31;
+  const int gl = lane >> 2, tig = lane & 3;
 
   const int C = p.k_split;
   const int rank = static_cast<int>(blockIdx.x % C);
-  const int64_t n0 = int64_t(blockIdx.x / C) * L::kWN;
-  const int64_t m0 = int64_t(blockIdx.y) * L::kMT;
-  const int64_t NW = p.N / 8;
-  const int64_t KS = p.K / 16;
+  const int64_t n0 = int64_t(blockIdx.x / C) * BN;
+  const int kb_begin = min(p.kb_total, rank * p.kb_per_cta);
+  const int nkb = min(p.kb_total, kb_begin + p.kb_per_cta) - kb_begin;
 
-  // K range of this CTA, then of this warp (contiguous pieces).
-  const int64_t c_begin = min64(KS, int64_t(rank) * p.ksteps_per_cta);
-  const int64_t c_end = min64(KS, c_begin + p.ksteps_per_cta);
-  const int64_t per_warp = (c_end - c_begin + kWarps - 1) / kWarps;
-  const int64_t w_begin = min64(c_end, c_begin + warp * per_warp);
-  const int64_t w_end = min64(c_end, w_begin + per_warp);
-  const int nsteps = static_cast<int>(w_end - w_begin);
+  const uint32_t full0 = base + L::kOffBar, empty0 = full0 + 8u * kStages;
+  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(base_ptr + L::kOffFlag);
+  const unsigned long long lim = g_decode_wait_limit_ns;
+  const uint64_t limit_ns = lim ? lim : kDefaultWaitNs;
 
-  uint8_t *ring = smem + warp * L::kWarpRing;
-  const uint32_t ring_u32 = smem_u32(ring);
-
-  // Inputs may be written by the previous kernel in the stream: wait for it before any global
-  // access, then let the next kernel start its launch while this one runs.
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, kConsumers);
+    }
+    *abort_flag = 0u;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  // Inputs may come from the previous kernel of the stream: wait for it before the first global
+  // access, then let the next kernel begin launching.
   griddep_wait();
   griddep_launch_dependents();
 
-  // ---- producer state: per-lane source pointers advanced by a fixed stride per k-step ----
-  // steps per scale group (G is a multiple of 16) and this warp's position inside its first group
-  const int spg = p.G / 16;
-  const int gpos0 = static_cast<int>(w_begin % spg);
-  const int64_t g_begin = w_begin / spg;
-  const int32_t *wsrc[V];
-  uint32_t wdst[V];
-  bool wok[V];
-#pragma unroll
-  for (int u = 0; u < V; ++u) {
-    const int ci = lane + 32 * u;
-    const int row = ci / (2 * V), c = ci % (2 * V);
-    const int64_t word = n0 / 8 + 4 * c;
-    wok[u] = word < NW;
-    wsrc[u] = p.b_q + (w_begin * 16 + row) * NW + (wok[u] ? word : 0);
-    wdst[u] = w_chunk_offset<V>(row, c);
-  }
-  constexpr int kAChunks = (2 * L::kMT + 31) / 32;
-  const uint16_t *asrc[kAChunks];
-  uint32_t adst[kAChunks];
-  bool aok[kAChunks], alane[kAChunks];
-#pragma unroll
-  for (int u = 0; u < kAChunks; ++u) {
-    const int ci = lane + 32 * u;
-    const int row = ci >> 1, c = ci & 1;
-    alane[u] = ci < 2 * L::kMT;
-    aok[u] = alane[u] && m0 + row < p.M;
-    asrc[u] = p.a + (aok[u] ? (m0 + row) * p.K + w_begin * 16 + 8 * c : 0);
-    adst[u] = L::kA + row * 32 + c * 16;
-  }
-  const bool s_lane = lane < L::kSBytes / 16;
-  const bool s_ok = s_lane && n0 + 8 * lane < p.N;
-  const uint16_t *ssrc = p.scales + g_begin * p.N + (s_ok ? n0 + 8 * lane : 0);
-  const bool z_lane = HAS_ZP && lane < L::kZBytes / 16;
-  const bool z_ok = z_lane && n0 / 8 + 4 * lane < NW;
-  const int32_t *zsrc = HAS_ZP ? p.qzeros + g_begin * NW + (z_ok ? n0 / 8 + 4 * lane : 0) : nullptr;
-  int issue_i = 0, issue_slot = 0, issue_gpos = gpos0;
-
-  // ---- producer: issue the copies of the next local step into its slot ----
-  auto issue = [&]() {
-    if (issue_i < nsteps) {
-      const uint32_t st = ring_u32 + issue_slot * L::kStage;
-#pragma unroll
-      for (int u = 0; u < V; ++u) {
-        cp_async_16(st + wdst[u], wsrc[u], wok[u]);
-        wsrc[u] += 16 * NW;
-      }
-#pragma unroll
-      for (int u = 0; u < kAChunks; ++u) {
-        if (alane[u]) cp_async_16(st + adst[u], asrc[u], aok[u]);
-        if (aok[u]) asrc[u] += 16;
-      }
-      if (issue_i == 0 || issue_gpos == 0) {
-        if (s_lane) cp_async_16(st + L::kS + 16 * lane, ssrc, s_ok);
-        if constexpr (HAS_ZP) {
-          if (z_lane) cp_async_16(st + L::kZ + 16 * lane, zsrc, z_ok);
-        }
-      }
-      if (++issue_gpos == spg) {
-        issue_gpos = 0;
-        ssrc += p.N;
-        if constexpr (HAS_ZP) zsrc += NW;
-      }
-      ++issue_i;
-      if (++issue_slot == kRing) issue_slot = 0;
-    }
-    cp_async_commit();
-  };
-
-  // ---- per-lane constant fragment addresses inside a stage ----
-  uint32_t w_off[4];
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int row = 4 * tig + r;
-    const int byte = 4 * V * gl;  // this lane's V words inside the row
-    w_off[r] = w_chunk_offset<V>(row, byte / 16) + (byte % 16);
-  }
-
-  // zero-point subtrahends (base + zp) per output column, packed twice (both k rows of a pair)
-  uint32_t zsub[V][8];
-  uint32_t s2[V][8];
-  auto make_zsub = [&](int j, uint32_t zp) -> uint32_t {
-    uint32_t h;
-    if constexpr (BF) h = 0x4300u | zp;               // 128 + zp
-    else h = (j & 1) ? (0x5400u | (zp << 4)) : (0x6400u | zp);  // 64 + zp  /  1024 + zp
-    return h | (h << 16);
-  };
-  if constexpr (!HAS_ZP) {
-#pragma unroll
-    for (int v = 0; v < V; ++v)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) zsub[v][j] = make_zsub(j, static_cast<uint32_t>(p.zp_bias));
-  }
-
-  float acc[J][V][4][4];
+  float acc[J][2][4];
 #pragma unroll
   for (int jt = 0; jt < J; ++jt)
 #pragma unroll
-    for (int v = 0; v < V; ++v)
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[jt][v][q][e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc[jt][q][e] = 0.f;
 
-  // ---- software pipeline ----
-#pragma unroll
-  for (int s = 0; s < kRing - 1; ++s) issue();
-
-  int slot = 0, gpos = gpos0;
-  for (int i = 0; i < nsteps; ++i) {
-    issue();
-    cp_async_wait<kRing - 1>();
-    __syncwarp();
-
-    const uint32_t st = ring_u32 + slot * L::kStage;
-    if (++slot == kRing) slot = 0;
-    const bool new_group = i == 0 || gpos == 0;
-    if (++gpos == spg) gpos = 0;
-
-    if (new_group) {
-      // scale row: this lane's 8V columns start at column 8*V*gl of the tile
-#pragma unroll
-      for (int v = 0; v < V; ++v) {
-        uint32_t sp[4];
-        lds128(st + L::kS + 16 * (V * gl + v), sp[0], sp[1], sp[2], sp[3]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s2[v][j] = prmt(sp[j >> 1], sp[j >> 1], (j & 1) ? 0x3232 : 0x1010);
+  if (warp == kConsumers) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t tx = L::kP + L::kA + kSRows * BN * 2 + (HAS_ZP ? kSRows * BN / 2 : 0);
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i & (kStages - 1);
+        if (!wait_phase(empty0 + 8u * s, ((i / kStages) & 1) ^ 1u, abort_flag, limit_ns, &g_decode_error)) break;
+        const uint32_t full = full0 + 8u * s;
+        mbar_arrive_expect_tx(full, tx);
+        const int k0 = (kb_begin + i) * BK;
+        const int grow = k0 / p.G;
+        tma_load_2d(base + L::kOffP + s * L::kP, &tmP, static_cast<int>(n0 / 8), k0, full);
+        tma_load_2d(base + L::kOffA + s * L::kA, &tmA, k0, 0, full);
+        tma_load_2d(base + L::kOffS + s * L::kS, &tmS, static_cast<int>(n0), grow, full);
+        if constexpr (HAS_ZP) tma_load_2d(base + L::kOffZ + s * L::kZ, &tmZ, static_cast<int>(n0 / 8), grow, full);
+        issued = i + 1;
       }
-      if constexpr (HAS_ZP) {
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-          const uint32_t zw = lds32(st + L::kZ + 4 * (V * gl + v));
-#pragma unroll
-          for (int j = 0; j < 8; ++j) zsub[v][j] = make_zsub(j, (zw >> (4 * j)) & 0xF);
-        }
+      if (*abort_flag) {
+        for (int i = issued - 1; i >= 0 && i >= issued - kStages; --i)
+          drain_phase(full0 + 8u * (i & (kStages - 1)), (i / kStages) & 1, &g_decode_error);
       }
     }
-
-    // activation fragments (B operand): A[row 8jt+gl][k 4tig .. 4tig+3]
-    uint32_t b0[J], b1[J];
-#pragma unroll
-    for (int jt = 0; jt < J; ++jt) lds64(st + L::kA + (8 * jt + gl) * 32 + 8 * tig, b0[jt], b1[jt]);
-
-    // packed weights: rows 4tig+r, this lane's V words
-    uint32_t w[4][V];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      if constexpr (V == 1) {
-        w[r][0] = lds32(st + w_off[r]);
-      } else if constexpr (V == 2) {
-        lds64(st + w_off[r], w[r][0], w[r][1]);
-      } else {
-        lds128(st + w_off[r], w[r][0], w[r][1], w[r][2], w[r][3]);
-      }
-    }
-
-#pragma unroll
-    for (int v = 0; v < V; ++v) {
-      // h[pair][j]: pair 0 = rows (4tig, 4tig+1), pair 1 = rows (4tig+2, 4tig+3); column 8(V gl + v) + j
-      uint32_t h[2][8];
-#pragma unroll
-      for (int pr = 0; pr < 2; ++pr) {
-        const uint32_t lo = prmt(w[2 * pr][v], w[2 * pr + 1][v], 0x5410);  // nibbles 0..3 of both rows
-        const uint32_t hi = prmt(w[2 * pr][v], w[2 * pr + 1][v], 0x7632);  // nibbles 4..7 of both rows
-        if constexpr (BF) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            h[pr][j] = and_or(lo >> (4 * j), 0x000F000Fu, 0x43004300u);
-            h[pr][j + 4] = and_or(hi >> (4 * j), 0x000F000Fu, 0x43004300u);
-          }
-        } else {
-          const uint32_t lo8 = lo >> 8, hi8 = hi >> 8;
-          h[pr][0] = and_or(lo, 0x000F000Fu, 0x64006400u);
-          h[pr][1] = and_or(lo, 0x00F000F0u, 0x54005400u);
-          h[pr][2] = and_or(lo8, 0x000F000Fu, 0x64006400u);
-          h[pr][3] = and_or(lo8, 0x00F000F0u, 0x54005400u);
-          h[pr][4] = and_or(hi, 0x000F000Fu, 0x64006400u);
-          h[pr][5] = and_or(hi, 0x00F000F0u, 0x54005400u);
-          h[pr][6] = and_or(hi8, 0x000F000Fu, 0x64006400u);
-          h[pr][7] = and_or(hi8, 0x00F000F0u, 0x54005400u);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) h[pr][j] = mul2_rn<BF>(sub2_rn<BF>(h[pr][j], zsub[v][j]), s2[v][j]);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        // MMA rows: gl -> column 8(V gl + v) + q ; gl + 8 -> column 8(V gl + v) + q + 4
-        const uint32_t af[4] = {h[0][q], h[0][q + 4], h[1][q], h[1][q + 4]};
-#pragma unroll
-        for (int jt = 0; jt < J; ++jt) mma_16816<BF>(acc[jt][v][q], af, b0[jt], b1[jt]);
-      }
-    }
-    __syncwarp();
-  }
-  cp_async_wait<0>();
-  __syncthreads();  // every warp is done with its ring: the ring area becomes the reduction buffer
-
-  // ---- reduction: warps (shared memory), then cluster ranks (distributed shared memory) ----
-  float *red = reinterpret_cast<float *>(smem);  // [kWarps][kMT][kWN]
-  constexpr int kTile = L::kMT * L::kWN;
-#pragma unroll
-  for (int jt = 0; jt < J; ++jt)
-#pragma unroll
-    for (int v = 0; v < V; ++v)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int n = 8 * (V * gl + v) + q;
-        const int m = 8 * jt + 2 * tig;
-        float *base = red + warp * kTile;
-        base[m * L::kWN + n] = acc[jt][v][q][0];
-        base[(m + 1) * L::kWN + n] = acc[jt][v][q][1];
-        base[m * L::kWN + n + 4] = acc[jt][v][q][2];
-        base[(m + 1) * L::kWN + n + 4] = acc[jt][v][q][3];
-      }
-  __syncthreads();
-
-  const int64_t rows_here = min64(L::kMT, p.M - m0);
-  for (int o = threadIdx.x; o < kTile; o += blockDim.x) {
-    if (o / L::kWN < rows_here) {
-      float s = 0.f;
-#pragma unroll
-      for (int wi = 0; wi < kWarps; ++wi) s += red[wi * kTile + o];
-      red[o] = s;
-    }
-  }
-
-  auto store = [&](int o, float v) {
-    const int m = o / L::kWN, n = o % L::kWN;
-    const int64_t gn = n0 + n;
-    if (m < rows_here && gn < p.N) {
-      if (p.bias) v += bits_to_float(p.bias[gn], BF);
-      const T y = DT::from_float_rn(v);
-      p.out[(m0 + m) * p.N + gn] = *reinterpret_cast<const uint16_t *>(&y);
-    }
-  };
-
-  if (C == 1) {
-    __syncthreads();
-    for (int o = threadIdx.x; o < kTile; o += blockDim.x) store(o, red[o]);
   } else {
-    cluster_sync_all();  // every rank's CTA sum is complete and visible cluster-wide
+    // ------------------------------------------------------------------ consumers
+    const int cb = warp;  // 16-byte chunk (32 columns) of every 128-byte packed row
+    // ldmatrix row addresses: lanes 8i..8i+7 -> matrix i, row (lane & 7)
+    const int mi = lane >> 3, rj = lane & 7;
+    const uint32_t p_off = uint32_t((8 * mi + rj) * 128 + ((cb ^ rj) << 4));          // row blocks 0..3
+    const uint32_t a_off = uint32_t(rj * 128 + ((mi ^ rj) << 4));                      // k chunks 0..3
+    const uint32_t a_off2 = uint32_t(rj * 128 + (((mi + 4) ^ rj) << 4));               // k chunks 4..7
+    const uint32_t s_off = uint32_t((32 * cb + 4 * gl) * 2);
+    const uint32_t z_off = uint32_t((4 * cb + (gl >> 1)) * 4);
+    const int z_shift = 16 * (gl & 1);
+
+    uint32_t s2[kSRows][4], zsub[kSRows][4];
+    if constexpr (!HAS_ZP) {
+#pragma unroll
+      for (int g = 0; g < kSRows; ++g)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) zsub[g][j] = zsub_of<BF>(j, static_cast<uint32_t>(p.zp_bias));
+    }
+    int gpos = (kb_begin % p.spg);
+    bool ok = true;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i & (kStages - 1);
+      ok = wait_phase(full0 + 8u * s, (i / kStages) & 1, abort_flag, limit_ns, &g_decode_error);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const uint32_t P = base + L::kOffP + s * L::kP;
+      const uint32_t A = base + L::kOffA + s * L::kA;
+      if (i == 0 || gpos == 0) {
+        const uint32_t S = base + L::kOffS + s * L::kS;
+#pragma unroll
+        for (int g = 0; g < kSRows; ++g) {
+          uint32_t s01, s23;
+          lds64(S + g * (BN * 2) + s_off, s01, s23);
+          s2[g][0] = prmt(s01, s01, 0x1010);
+          s2[g][1] = prmt(s01, s01, 0x3232);
+          s2[g][2] = prmt(s23, s23, 0x1010);
+          s2[g][3] = prmt(s23, s23, 0x3232);
+          if constexpr (HAS_ZP) {
+            const uint32_t Z = base + L::kOffZ + s * L::kZ;
+            const uint32_t z16 = lds32(Z + g * (BN / 2) + z_off) >> z_shift;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) zsub[g][j] = zsub_of<BF>(j, (z16 >> (4 * j)) & 0xFu);
+          }
+        }
+      }
+      if (++gpos == p.spg) gpos = 0;
+
+      uint32_t wq[8];        // row blocks 0..7 of column block cb
+      uint32_t af[J][8];     // B fragments: (b0, b1) for k16 steps 0..3
+      {
+        uint32_t r[4];
+        ldsm_x4_trans(P + p_off, r);
+        wq[0] = r[0]; wq[1] = r[1]; wq[2] = r[2]; wq[3] = r[3];
+        ldsm_x4_trans(P + p_off + 4096u, r);
+        wq[4] = r[0]; wq[5] = r[1]; wq[6] = r[2]; wq[7] = r[3];
+#pragma unroll
+        for (int jt = 0; jt < J; ++jt) {
+          ldsm_x4(A + jt * 1024u + a_off, r);
+          af[jt][0] = r[0]; af[jt][1] = r[1]; af[jt][2] = r[2]; af[jt][3] = r[3];
+          ldsm_x4(A + jt * 1024u + a_off2, r);
+          af[jt][4] = r[0]; af[jt][5] = r[1]; af[jt][6] = r[2]; af[jt][7] = r[3];
+        }
+      }
+      // every value this warp needs from the stage is in registers: release the stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8u * s);
+
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int g = (TWO_GROUPS && t >= 2) ? 1 : 0;  // rows 32..63 belong to the second group
+        uint32_t lo[4], hi[4];
+        magic_quad<BF>(wq[2 * t], lo);
+        magic_quad<BF>(wq[2 * t + 1], hi);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          lo[j] = mul2_rn<BF>(sub2_rn<BF>(lo[j], zsub[g][j]), s2[g][j]);
+          hi[j] = mul2_rn<BF>(sub2_rn<BF>(hi[j], zsub[g][j]), s2[g][j]);
+        }
+        // MMA rows: g -> column 4*gl + j, g + 8 -> column 4*gl + j + 2, for j = 0 and j = 1
+        const uint32_t a0[4] = {lo[0], lo[2], hi[0], hi[2]};
+        const uint32_t a1[4] = {lo[1], lo[3], hi[1], hi[3]};
+#pragma unroll
+        for (int jt = 0; jt < J; ++jt) {
+          mma_16816<BF>(acc[jt][0], a0, af[jt][2 * t], af[jt][2 * t + 1]);
+          mma_16816<BF>(acc[jt][1], a1, af[jt][2 * t], af[jt][2 * t + 1]);
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ reduction and epilogue
+  const int64_t rows = p.M < 8 * J ? p.M : 8 * J;
+  auto finish = [&](int m, int64_t n, float v) {
+    if (m < rows && n < p.N) {
+      if (p.bias) v += bits_to_float(p.bias[n], BF);
+      const T y = DT::from_float_rn(v);
+      p.out[m * p.N + n] = *reinterpret_cast<const uint16_t *>(&y);
+    }
+  };
+  if (C == 1) {
+    if (warp < kConsumers) {
+      const int64_t nb = n0 + 32 * warp + 4 * gl;
+#pragma unroll
+      for (int jt = 0; jt < J; ++jt)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int m = 8 * jt + 2 * tig;
+          finish(m, nb + q, acc[jt][q][0]);
+          finish(m + 1, nb + q, acc[jt][q][1]);
+          finish(m, nb + q + 2, acc[jt][q][2]);
+          finish(m + 1, nb + q + 2, acc[jt][q][3]);
+        }
+    }
+  } else {
+    __syncthreads();  // all stages consumed and all copies landed: the weight ring becomes red[m][n]
+    float *red = reinterpret_cast<float *>(base_ptr + L::kOffP);
+    if (warp < kConsumers) {
+      const int nl = 32 * warp + 4 * gl;
+#pragma unroll
+      for (int jt = 0; jt < J; ++jt)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int m = 8 * jt + 2 * tig;
+          red[m * BN + nl + q] = acc[jt][q][0];
+          red[(m + 1) * BN + nl + q] = acc[jt][q][1];
+          red[m * BN + nl + q + 2] = acc[jt][q][2];
+          red[(m + 1) * BN + nl + q + 2] = acc[jt][q][3];
+        }
+    }
+    cluster_sync_all();  // every rank's partial tile is complete and visible cluster-wide
+    constexpr int kTile = 8 * J * BN;
     const int per = (kTile + C - 1) / C;
-    const int o_begin = rank * per, o_end = o_begin + per < kTile ? o_begin + per : kTile;
-    const uint32_t red_u32 = smem_u32(red);
-    for (int o = o_begin + threadIdx.x; o < o_end; o += blockDim.x) {
-      if (o / L::kWN < rows_here) {
-        float s = 0.f;
-        for (int rr = 0; rr < C; ++rr) s += ld_dsmem_f32(map_to_rank(red_u32 + 4u * o, rr));
-        store(o, s);
+    const int o_begin = rank * per;
+    const int o_end = o_begin + per < kTile ? o_begin + per : kTile;
+    const uint32_t red_u32 = base + L::kOffP;
+    for (int o = o_begin + threadIdx.x; o < o_end; o += kThreads) {
+      const int m = o / BN;
+      if (m < rows) {
+        float v = 0.f;
+        for (int rr = 0; rr < C; ++rr) v += ld_dsmem_f32(map_to_rank(red_u32 + 4u * o, rr));
+        finish(m, n0 + (o % BN), v);
       }
     }
     cluster_sync_all();  // keep this CTA's shared memory alive until every rank has read it
@@ -380,35 +332,17 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 // ---------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------
-using KernelFn = void (*)(const DecodeParams);
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                          const DecodeParams);
 
-template <class DT, int V, int J, bool Z>
-KernelFn kernel_ptr() {
-  return decode_kernel<DT, V, J, Z>;
+template <class DT, int J>
+KernelFn pick_zg(bool zp, bool two) {
+  if (zp) return two ? decode_kernel<DT, J, true, true> : decode_kernel<DT, J, true, false>;
+  return two ? decode_kernel<DT, J, false, true> : decode_kernel<DT, J, false, false>;
 }
-template <int V, int J, bool Z>
-int smem_bytes() {
-  return DecodeLayout<V, J, Z>::kSmem;
-}
-
-struct Variant {
-  KernelFn fn;
-  int smem;
-};
-
-template <class DT, bool Z>
-Variant pick_vj(int V, int J) {
-  if (J == 1) {
-    if (V == 1) return {kernel_ptr<DT, 1, 1, Z>(), smem_bytes<1, 1, Z>()};
-    return {kernel_ptr<DT, 2, 1, Z>(), smem_bytes<2, 1, Z>()};
-  }
-  if (J == 2) return {kernel_ptr<DT, 1, 2, Z>(), smem_bytes<1, 2, Z>()};
-  return {kernel_ptr<DT, 1, 4, Z>(), smem_bytes<1, 4, Z>()};
-}
-
-Variant pick(int dtype, bool has_zp, int V, int J) {
-  if (dtype == W4A16_BF16) return has_zp ? pick_vj<BF16, true>(V, J) : pick_vj<BF16, false>(V, J);
-  return has_zp ? pick_vj<F16, true>(V, J) : pick_vj<F16, false>(V, J);
+KernelFn pick(int dtype, int J, bool zp, bool two) {
+  if (dtype == W4A16_BF16) return J == 1 ? pick_zg<BF16, 1>(zp, two) : pick_zg<BF16, 2>(zp, two);
+  return J == 1 ? pick_zg<F16, 1>(zp, two) : pick_zg<F16, 2>(zp, two);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -416,74 +350,75 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace
 
 bool decode_supported(const GemmArgs &g) {
-  return g.N % 32 == 0 && g.K % 16 == 0 && g.group_size % 16 == 0 && aligned16(g.a) &&
-         aligned16(g.b_q) && aligned16(g.scales) && (g.qzeros == nullptr || aligned16(g.qzeros));
+  return g.M <= 16 && g.N % 32 == 0 && g.K % 8 == 0 && aligned16(g.a) && aligned16(g.b_q) &&
+         aligned16(g.scales) && (g.qzeros == nullptr || aligned16(g.qzeros));
 }
 
-void decode_make_plan(int64_t M, int64_t K, int64_t N, int has_zp, int num_sms, w4a16_plan_t *p) {
-  const int J = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
-  const int64_t KS = K / 16;
-  const int64_t m_tiles = (M + 8 * J - 1) / (8 * J);
-  // Two CTAs of 8 warps fit on an SM (registers and shared memory): aim for one such wave.
+void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, w4a16_plan_t *p) {
+  (void)group_size;
+  const int J = M <= 8 ? 1 : 2;
+  const int64_t n_tiles = (N + BN - 1) / BN;
+  const int64_t kbt = (K + BK - 1) / BK;
+  // two CTAs fit on an SM: aim for one such wave; every cluster rank keeps at least two K blocks
   const int64_t slots = 2 * int64_t(num_sms);
-  int bestV = 1, bestC = 1;
+  int bestC = 1;
   double best = -1.0;
-  for (int V = 2; V >= 1; --V) {
-    if (J > 1 && V != 1) continue;  // multi-tile rows: one word per lane keeps registers in check
-    const int64_t n_tiles = (N + 64 * V - 1) / (64 * V);
-    for (int C = 1; C <= 8; ++C) {
-      if (C > 1 && KS < int64_t(C) * kWarps) break;  // every warp keeps at least one k-step
-      const int64_t ctas = n_tiles * C * m_tiles;
-      const int64_t waves = (ctas + slots - 1) / slots;
-      double eff = double(ctas) / double(waves * slots);
-      if (V == 2) eff *= 1.08;  // wider loads and fewer column tiles: preferred at equal fill
-      if (eff > best + 1e-9) {
-        best = eff;
-        bestV = V;
-        bestC = C;
-      }
+  for (int C = 1; C <= 8; ++C) {
+    if (C > 1 && kbt < 2 * int64_t(C)) break;
+    const int64_t ctas = n_tiles * C;
+    const int64_t waves = (ctas + slots - 1) / slots;
+    const double eff = double(ctas) / double(waves * slots);
+    if (eff > best + 1e-9) {
+      best = eff;
+      bestC = C;
     }
   }
-  const int V = bestV;
   const int64_t C = bestC;
-  const int64_t n_tiles = (N + 64 * V - 1) / (64 * V);
-  const int64_t kc = (KS + C - 1) / C;
   p->path = W4A16_PATH_DECODE;
-  p->words_per_lane = V;
+  p->words_per_lane = 1;
   p->m_tile = 8 * J;
-  p->n_tile = 64 * V;
+  p->n_tile = BN;
   p->k_split = static_cast<int32_t>(C);
-  p->warps = kWarps;
-  p->grid = n_tiles * C * m_tiles;
-  p->smem_bytes = pick(W4A16_F16, has_zp != 0, V, J).smem;
-  p->reserved = static_cast<int32_t>(kc);
+  p->warps = kConsumers + 1;
+  p->grid = n_tiles * C;
+  p->smem_bytes = J == 1 ? Layout<1>::kSmem : Layout<2>::kSmem;
+  p->reserved = static_cast<int32_t>((kbt + C - 1) / C);
 }
 
 cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
-  const int V = pl.words_per_lane, J = pl.m_tile / 8, C = pl.k_split;
-  const Variant var = pick(g.dtype, g.qzeros != nullptr, V, J);
-
-  static std::mutex mu;
-  static bool configured[64][2][2][5] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  const int J = pl.m_tile / 8;
+  const int C = pl.k_split;
+  const bool zp = g.qzeros != nullptr;
+  const bool two = g.group_size < BK && g.group_size != g.K;  // G = 32: two groups per K block
+  const int srows = two ? 2 : 1;
+  const int64_t NW = g.N / 8, ng = g.K / g.group_size;
+  CUtensorMap tA, tP, tS, tZ;
+  if (!tma_encode_2d(&tA, 2, g.a, g.K, g.M, g.K * 2, BK, 8 * J, true) ||
+      !tma_encode_2d(&tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK, true) ||
+      !tma_encode_2d(&tS, 2, g.scales, g.N, ng, g.N * 2, BN, srows, false))
+    return cudaErrorInvalidValue;
+  if (zp) {
+    if (!tma_encode_2d(&tZ, 4, g.qzeros, NW, ng, NW * 4, BN / 8, srows, false)) return cudaErrorInvalidValue;
+  } else {
+    tZ = tP;  // unused
+  }
+  const KernelFn fn = pick(g.dtype, J, zp, two);
+  const int smem = J == 1 ? Layout<1>::kSmem : Layout<2>::kSmem;
   {
-    const int vi = V == 1 ? (J == 1 ? 0 : (J == 2 ? 3 : 4)) : 1;
+    static std::mutex mu;
+    static bool configured[64][2][2][2][2] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
-    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][g.qzeros != nullptr][vi];
+    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][J - 1][zp][two];
     if (!done) {
-      e = cudaFuncSetAttribute(var.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, var.smem);
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       done = true;
     }
   }
-
   DecodeParams prm;
-  prm.a = static_cast<const uint16_t *>(g.a);
-  prm.b_q = g.b_q;
-  prm.scales = static_cast<const uint16_t *>(g.scales);
-  prm.qzeros = g.qzeros;
   prm.bias = static_cast<const uint16_t *>(g.bias);
   prm.out = static_cast<uint16_t *>(g.out);
   prm.M = g.M;
@@ -492,16 +427,15 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
   prm.G = g.group_size;
   prm.zp_bias = g.zp_bias;
   prm.k_split = C;
-  const int64_t KS = g.K / 16;
-  prm.ksteps_per_cta = static_cast<int>((KS + C - 1) / C);
+  prm.kb_total = static_cast<int>((g.K + BK - 1) / BK);
+  prm.kb_per_cta = (prm.kb_total + C - 1) / C;
+  prm.spg = g.group_size >= BK ? g.group_size / BK : 1;
 
-  const int64_t n_tiles = (g.N + 64 * V - 1) / (64 * V);
-  const int64_t m_tiles = (g.M + 8 * J - 1) / (8 * J);
-
+  const int64_t n_tiles = (g.N + BN - 1) / BN;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(n_tiles * C), static_cast<unsigned>(m_tiles), 1);
-  cfg.blockDim = dim3(kWarps * 32, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(var.smem);
+  cfg.gridDim = dim3(static_cast<unsigned>(n_tiles * C), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = g.stream;
   cudaLaunchAttribute attr[2];
   int nattr = 0;
@@ -517,10 +451,24 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
-  e = cudaLaunchKernelEx(&cfg, var.fn, prm);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tA, tP, tS, tZ, prm);
   if (e != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;
+}
+
+cudaError_t decode_take_device_error(uint32_t *err) {
+  uint32_t v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_decode_error, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v) e = cudaMemcpyToSymbol(g_decode_error, &zero, sizeof(zero));
+  *err = v;
+  return e;
+}
+
+cudaError_t decode_set_wait_limit_ns(uint64_t ns) {
+  const unsigned long long v = ns;
+  return cudaMemcpyToSymbol(g_decode_wait_limit_ns, &v, sizeof(v));
 }
 
 }  // namespace w4a16

@@ -25,8 +25,6 @@
 //    TMEM and exits without writing output.
 //  * Epilogue: tcgen05.ld 32 columns at a time, + bias in fp32, one rounding to the dtype, 16-byte
 //    stores (PR #40977 report, key source snippets, test reference: bias before the cast).
-#include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched from the driver at run time
-
 #include <mutex>
 
 #include "common.cuh"
@@ -62,7 +60,6 @@ static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0 && kABytes % 1024 == 0, "
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
-constexpr uint64_t kDrainWaitNs = 1000000000ull;    // 1 s, for draining own copies after an abort
 
 __device__ unsigned int g_prefill_error;
 __device__ unsigned long long g_wait_limit_ns;
@@ -70,37 +67,6 @@ __device__ unsigned long long g_wait_limit_ns;
 // ---------------------------------------------------------------------------------------------
 // PTX wrappers: mbarrier, TMA, tcgen05
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
@@ -145,32 +111,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Bounded wait on an mbarrier phase. Returns false if this CTA is aborting (flag set here on timeout).
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                           uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer() - t0 > limit_ns) {
-      *abort_flag = 1u;
-      atomicOr(&g_prefill_error, 1u);
-      return false;
-    }
-  }
-}
-// Drain wait after an abort: ignores the abort flag, fixed bound.
-__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kDrainWaitNs) {
-      atomicOr(&g_prefill_error, 2u);
-      return;
-    }
-  }
-}
-
 struct PrefillParams {
   const uint16_t *bias;
   uint16_t *out;
@@ -178,7 +118,6 @@ struct PrefillParams {
   int G;
   int zp_bias;
   int nk;     // K blocks of 64
-  int srows;  // scale / zero-point rows loaded per K block (2 when a block can span two groups)
 };
 
 template <bool BF>
@@ -198,7 +137,7 @@ __device__ __forceinline__ void magic4(uint32_t w, uint32_t (&h)[4]) {
   }
 }
 
-template <class DT, bool HAS_ZP>
+template <class DT, bool HAS_ZP, bool TWO_GROUPS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmP,
                    const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ,
@@ -237,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(accum_full, 1);
     *abort_flag = 0u;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   if (warp == 1) tmem_alloc(slot, kTmemCols);
   tc_fence_before();
@@ -246,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(base_ptr + kOffSlot);
 
   const int nk = p.nk;
-  const int srows = p.srows;
+  constexpr int srows = TWO_GROUPS ? 2 : 1;  // G = 32: a K block spans two scale groups
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -256,10 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % SA;
         const uint32_t ph = (kb / SA) & 1;
-        if (!wait_phase(empty_a(s), ph ^ 1u, abort_flag, limit_ns)) break;
+        if (!wait_phase(empty_a(s), ph ^ 1u, abort_flag, limit_ns, &g_prefill_error)) break;
         mbar_arrive_expect_tx(full_a(s), tx);
         const int k0 = kb * BK;
-        const int grow = static_cast<int>(int64_t(k0) / p.G);
+        const int grow = k0 / p.G;
         tma_load_2d(base + kOffA + s * kABytes, &tmA, k0, static_cast<int>(m0), full_a(s));
         tma_load_2d(base + kOffP + s * kPBytes, &tmP, static_cast<int>(n0 / 8), k0, full_a(s));
         tma_load_2d(base + kOffS + s * kSBytes, &tmS, static_cast<int>(n0), grow, full_a(s));
@@ -268,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (*abort_flag) {
         // let this CTA's own copies land before its shared memory is released
-        for (int kb = issued - 1; kb >= 0 && kb >= issued - SA; --kb) drain_phase(full_a(kb % SA), (kb / SA) & 1);
+        for (int kb = issued - 1; kb >= 0 && kb >= issued - SA; --kb) drain_phase(full_a(kb % SA), (kb / SA) & 1, &g_prefill_error);
       }
     }
   } else if (warp == 1) {
@@ -284,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int kb = 0; kb < nk && ok; ++kb) {
         const int sa = kb % SA, sb = kb % SB;
-        ok = wait_phase(full_a(sa), (kb / SA) & 1, abort_flag, limit_ns) &&
-             wait_phase(full_b(sb), (kb / SB) & 1, abort_flag, limit_ns);
+        ok = wait_phase(full_a(sa), (kb / SA) & 1, abort_flag, limit_ns, &g_prefill_error) &&
+             wait_phase(full_b(sb), (kb / SB) & 1, abort_flag, limit_ns, &g_prefill_error);
         if (!ok) break;
         tc_fence_after();
         const uint32_t a_base = base + kOffA + sa * kABytes;
@@ -303,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(empty_b(sb));
       }
       umma_commit(accum_full);
-      if (!ok) drain_phase(accum_full, 0);
+      if (!ok) drain_phase(accum_full, 0, &g_prefill_error);
     }
   } else {
     // ------------------------------------------------------------ dequantisers
@@ -324,16 +263,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int kb = 0; kb < nk; ++kb) {
       const int sa = kb % SA, sb = kb % SB;
-      ok = wait_phase(full_a(sa), (kb / SA) & 1, abort_flag, limit_ns) &&
-           wait_phase(empty_b(sb), ((kb / SB) & 1) ^ 1u, abort_flag, limit_ns);
+      ok = wait_phase(full_a(sa), (kb / SA) & 1, abort_flag, limit_ns, &g_prefill_error) &&
+           wait_phase(empty_b(sb), ((kb / SB) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error);
       ok = __all_sync(0xffffffffu, ok);  // the warp leaves the loop together
       if (!ok) break;
       const uint32_t P = base + kOffP + sa * kPBytes;
       const uint32_t S = base + kOffS + sa * kSBytes;
       const uint32_t Z = base + kOffZ + sa * kZBytes;
       const uint32_t B = base + kOffB + sb * kBBytes;
-      const int64_t k0 = int64_t(kb) * BK;
-      const int64_t g0 = k0 / p.G;
 #pragma unroll
       for (int gr = 0; gr < 2; ++gr) {
         if (gr < srows) {
@@ -349,17 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < BK / kDequantWarps; ++i) {
         const int r = dw + kDequantWarps * i;
-        int gr = srows == 2 ? static_cast<int>((k0 + r) / p.G - g0) : 0;
-        gr = gr > 1 ? 1 : gr;
+        const int gr = (TWO_GROUPS && i >= BK / kDequantWarps / 2) ? 1 : 0;  // rows 32..63: second group
         const uint32_t wq = lds32(P + r * (BN / 2) + c * 4);
         uint32_t h[4];
         magic4<BF>(wq, h);
         uint32_t x[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t zz = gr ? zsub[1][j] : zsub[0][j];
-          const uint32_t ss = gr ? spair[1][j] : spair[0][j];
-          x[j] = mul2_rn<BF>(sub2_rn<BF>(h[j], zz), ss);
+          x[j] = mul2_rn<BF>(sub2_rn<BF>(h[j], zsub[gr][j]), spair[gr][j]);
         }
         // MN-major, 128-byte swizzle: 8-row K groups 4096 B apart, 64-column atoms 1024 B apart,
         // row r%8 at 128 B, 16-byte chunk (c%8) XOR (r%8).
@@ -375,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok) ok = wait_phase(accum_full, 0, abort_flag, limit_ns);
+    if (ok) ok = wait_phase(accum_full, 0, abort_flag, limit_ns, &g_prefill_error);
     ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
     tc_fence_after();
     const int q = warp & 3;                // TMEM lane quarter this warp may read
@@ -444,42 +378,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------
-using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn encoder() {
-  static EncodeFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(ptr);
-  });
-  return fn;
-}
-
-bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t inner, uint64_t outer,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return encoder()(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                           const PrefillParams);
 
-KernelFn pick(int dtype, bool zp) {
-  if (dtype == W4A16_BF16) return zp ? prefill_kernel<BF16, true> : prefill_kernel<BF16, false>;
-  return zp ? prefill_kernel<F16, true> : prefill_kernel<F16, false>;
+template <class DT>
+KernelFn pick_dt(bool zp, bool two) {
+  if (zp) return two ? prefill_kernel<DT, true, true> : prefill_kernel<DT, true, false>;
+  return two ? prefill_kernel<DT, false, true> : prefill_kernel<DT, false, false>;
+}
+KernelFn pick(int dtype, bool zp, bool two) {
+  return dtype == W4A16_BF16 ? pick_dt<BF16>(zp, two) : pick_dt<F16>(zp, two);
 }
 
 }  // namespace
@@ -487,7 +397,7 @@ KernelFn pick(int dtype, bool zp) {
 bool prefill_supported(const GemmArgs &g) {
   return g.N % 32 == 0 && g.K % 8 == 0 && aligned16(g.a) && aligned16(g.b_q) && aligned16(g.scales) &&
          aligned16(g.out) && (g.qzeros == nullptr || aligned16(g.qzeros)) && (g.bias == nullptr || aligned16(g.bias)) &&
-         (g.N + BN - 1) / BN <= 65535 && encoder() != nullptr;
+         (g.N + BN - 1) / BN <= 65535;
 }
 
 void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, w4a16_plan_t *p) {
@@ -508,28 +418,27 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
 cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &) {
   const bool zp = g.qzeros != nullptr;
   const int64_t NW = g.N / 8, ng = g.K / g.group_size;
-  const int srows = g.group_size < BK ? 2 : 1;
+  const bool two = g.group_size < BK && g.group_size != g.K;  // G = 32: two groups per K block
+  const int srows = two ? 2 : 1;
   CUtensorMap tA, tP, tS, tZ;
-  if (!encode_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.a, g.K, g.M, g.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tP, CU_TENSOR_MAP_DATA_TYPE_INT32, g.b_q, NW, g.K, NW * 4, BN / 8, BK, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !encode_2d(&tS, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.scales, g.N, ng, g.N * 2, BN, srows, CU_TENSOR_MAP_SWIZZLE_NONE))
+  if (!tma_encode_2d(&tA, 2, g.a, g.K, g.M, g.K * 2, BK, BM, true) ||
+      !tma_encode_2d(&tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK, false) ||
+      !tma_encode_2d(&tS, 2, g.scales, g.N, ng, g.N * 2, BN, srows, false))
     return cudaErrorInvalidValue;
   if (zp) {
-    if (!encode_2d(&tZ, CU_TENSOR_MAP_DATA_TYPE_INT32, g.qzeros, NW, ng, NW * 4, BN / 8, srows,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
-      return cudaErrorInvalidValue;
+    if (!tma_encode_2d(&tZ, 4, g.qzeros, NW, ng, NW * 4, BN / 8, srows, false)) return cudaErrorInvalidValue;
   } else {
     tZ = tP;  // unused
   }
-  const KernelFn fn = pick(g.dtype, zp);
+  const KernelFn fn = pick(g.dtype, zp, two);
   {
     static std::mutex mu;
-    static bool configured[64][2][2] = {};
+    static bool configured[64][2][2][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
-    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][zp];
+    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][zp][two];
     if (!done) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
       if (e != cudaSuccess) return e;
@@ -545,7 +454,6 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &) {
   prm.G = g.group_size;
   prm.zp_bias = g.zp_bias;
   prm.nk = static_cast<int>((g.K + BK - 1) / BK);
-  prm.srows = srows;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((g.M + BM - 1) / BM), static_cast<unsigned>((g.N + BN - 1) / BN), 1);

@@ -1,6 +1,7 @@
 // Host-side interfaces between the translation units of libw4a16.so (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (types only; the encoder is fetched from the driver at run time)
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -35,6 +36,13 @@ cudaError_t current_device_info(DeviceInfo *info);
 // Records one kernel launch in the process-wide counter.
 void note_launch();
 
+// 2-D tiled TMA descriptor over a row-major [outer, inner] tensor (inner contiguous), box
+// [box_outer, box_inner], zero fill outside the tensor. elem_bytes is 2 or 4. Returns false when the
+// driver rejects it or the encoder is unavailable.
+bool tma_encode_2d(CUtensorMap *map, int elem_bytes, const void *ptr, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle_128b);
+bool tma_available();
+
 cudaError_t launch_pack(const uint8_t *q, int32_t *packed, int64_t rows, int64_t n, cudaStream_t s);
 cudaError_t launch_unpack(const int32_t *packed, uint8_t *q, int64_t rows, int64_t n, cudaStream_t s);
 cudaError_t launch_dequant(const int32_t *b_q, const void *scales, const int32_t *qzeros, int64_t k,
@@ -43,10 +51,12 @@ cudaError_t launch_dequant(const int32_t *b_q, const void *scales, const int32_t
 
 cudaError_t launch_gemm_generic(const GemmArgs &g);
 
-// Decode path: plan fields words_per_lane, m_tile, k_split, warps are honoured.
+// Decode path (M <= 16): plan fields m_tile and k_split are honoured.
 bool decode_supported(const GemmArgs &g);
-void decode_make_plan(int64_t M, int64_t K, int64_t N, int has_zp, int num_sms, w4a16_plan_t *p);
+void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, w4a16_plan_t *p);
 cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &p);
+cudaError_t decode_take_device_error(uint32_t *err);
+cudaError_t decode_set_wait_limit_ns(uint64_t ns);
 
 // Prefill path (tcgen05).
 bool prefill_supported(const GemmArgs &g);
