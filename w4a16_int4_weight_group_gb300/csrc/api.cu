@@ -90,7 +90,7 @@ int forced_path() {
 constexpr int64_t kPrefillMinM = 65;
 
 // `tma` tells whether the driver's tensor-map encoder is available (the TMA-fed paths need it).
-void choose_plan(const GemmArgs &g, int num_sms, bool tma, w4a16_plan_t *p) {
+void choose_plan(const GemmArgs &g, int num_sms, bool tma, bool query_device, w4a16_plan_t *p) {
   std::memset(p, 0, sizeof(*p));
   if (g.M == 0) {
     p->path = W4A16_PATH_NONE;
@@ -114,7 +114,7 @@ void choose_plan(const GemmArgs &g, int num_sms, bool tma, w4a16_plan_t *p) {
     path = W4A16_PATH_GENERIC;
   }
   if (path == W4A16_PATH_DECODE) {
-    decode_make_plan(g.M, g.K, g.N, g.group_size, num_sms, p);
+    decode_make_plan(g.M, g.K, g.N, g.group_size, num_sms, query_device, p);
   } else if (path == W4A16_PATH_PREFILL) {
     prefill_make_plan(g.M, g.K, g.N, g.group_size, num_sms, p);
   } else {
@@ -305,7 +305,7 @@ w4a16_status w4a16_gemm(const void *a, const int32_t *b_q, const void *scales, c
   cudaError_t e = current_device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "device query");
   w4a16_plan_t plan;
-  choose_plan(g, dev.num_sms, tma_available(), &plan);
+  choose_plan(g, dev.num_sms, tma_available(), /*query_device=*/true, &plan);
   switch (plan.path) {
     case W4A16_PATH_DECODE: e = launch_gemm_decode(g, plan); break;
     case W4A16_PATH_PREFILL: e = launch_gemm_prefill(g, plan); break;
@@ -321,6 +321,7 @@ w4a16_status w4a16_plan(int64_t m, int64_t k, int64_t n, int group_size, int dty
   w4a16_status st = check_config(k, n, group_size, dtype);
   if (st != W4A16_OK) return st;
   if (m < 0 || m >= kMaxDim) return fail(W4A16_ERR_INVALID_ARG, "M (%lld) must be in [0, 2^31)", (long long)m);
+  const bool query_device = num_sms <= 0;
   if (num_sms <= 0) {
     DeviceInfo dev;
     cudaError_t e = current_device_info(&dev);
@@ -333,7 +334,8 @@ w4a16_status w4a16_plan(int64_t m, int64_t k, int64_t n, int group_size, int dty
       (reinterpret_cast<uintptr_t>(kAlignedWord) + 15) & ~uintptr_t(15));
   GemmArgs g{p16, static_cast<const int32_t *>(p16), p16, has_zp ? static_cast<const int32_t *>(p16) : nullptr,
              group_size, 8, nullptr, nullptr, m, k, n, dtype, nullptr};
-  choose_plan(g, num_sms, /*tma=*/true, plan);  // a host-only query: assume a GPU driver
+  // a host-only query: assume a GPU driver; use the device's occupancy only when it was asked for
+  choose_plan(g, num_sms, /*tma=*/true, query_device, plan);
   return ok();
 }
 

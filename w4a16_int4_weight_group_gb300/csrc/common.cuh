@@ -146,9 +146,11 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
   return r;
 }
+// Plain (non-volatile) load so that the compiler may issue several remote loads back to back; the
+// ordering against the writers comes from the cluster barrier that precedes the reads.
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr));
   return v;
 }
 
@@ -198,10 +200,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.p
 // kernel's device error word; it also returns false early once another thread has set the flag.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                            uint64_t limit_ns, unsigned int *error_word) {
-  if (mbar_try_wait(bar, parity)) return true;
+  // the suspend hint never exceeds the limit, so a short limit is honoured promptly
+  const uint32_t hint = limit_ns < 1000u ? static_cast<uint32_t>(limit_ns) : 1000u;
+  if (mbar_try_wait(bar, parity, hint)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, hint)) return true;
     if (*abort_flag) return false;
     if (globaltimer() - t0 > limit_ns) {
       *abort_flag = 1u;

@@ -320,8 +320,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int o = o_begin + threadIdx.x; o < o_end; o += kThreads) {
       const int m = o / BN;
       if (m < rows) {
+        // issue every rank's load before summing (in rank order: deterministic)
+        float part[8];
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) part[rr] = rr < C ? ld_dsmem_f32(map_to_rank(red_u32 + 4u * o, rr)) : 0.f;
         float v = 0.f;
-        for (int rr = 0; rr < C; ++rr) v += ld_dsmem_f32(map_to_rank(red_u32 + 4u * o, rr));
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) v += part[rr];
         finish(m, n0 + (o % BN), v);
       }
     }
@@ -347,27 +352,72 @@ KernelFn pick(int dtype, int J, bool zp, bool two) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-}  // namespace
-
-bool decode_supported(const GemmArgs &g) {
+bool decode_supported_impl(const GemmArgs &g) {
   return g.M <= 16 && g.N % 32 == 0 && g.K % 8 == 0 && aligned16(g.a) && aligned16(g.b_q) &&
          aligned16(g.scales) && (g.qzeros == nullptr || aligned16(g.qzeros));
 }
 
-void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, w4a16_plan_t *p) {
+// CTAs of one decode kernel that can be resident at once when launched in clusters of C
+// (0 when unknown: no device). Queried from the runtime once per device and cluster size.
+int64_t resident_ctas(int J, int C) {
+  static std::mutex mu;
+  static int cache[64][2][9];
+  static bool have[64][2][9] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[dev][J - 1][C]) {
+    const KernelFn fn = pick(W4A16_F16, J, true, false);
+    const int smem = J == 1 ? Layout<1>::kSmem : Layout<2>::kSmem;
+    int n = 0;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+      if (C == 1) {
+        int per_sm = 0, sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+          n = per_sm * sms;
+      } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(C), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(C);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess) n = clusters * C;
+      }
+    }
+    cudaGetLastError();  // a failed query leaves no sticky state
+    cache[dev][J - 1][C] = n;
+    have[dev][J - 1][C] = true;
+  }
+  return cache[dev][J - 1][C];
+}
+
+}  // namespace
+
+void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool query_device,
+                      w4a16_plan_t *p) {
   (void)group_size;
   const int J = M <= 8 ? 1 : 2;
   const int64_t n_tiles = (N + BN - 1) / BN;
   const int64_t kbt = (K + BK - 1) / BK;
-  // two CTAs fit on an SM: aim for one such wave; every cluster rank keeps at least two K blocks
-  const int64_t slots = 2 * int64_t(num_sms);
+  // Choose the cluster size C (split-K factor) that keeps the most CTAs busy in full waves; the
+  // resident count comes from the runtime's occupancy query (two CTAs per SM when unknown).
   int bestC = 1;
   double best = -1.0;
   for (int C = 1; C <= 8; ++C) {
-    if (C > 1 && kbt < 2 * int64_t(C)) break;
+    if (C > 1 && kbt < 2 * int64_t(C)) break;  // every rank keeps at least two K blocks
+    int64_t slots = query_device ? resident_ctas(J, C) : 0;
+    if (slots <= 0) slots = 2 * int64_t(num_sms) / C * C;
     const int64_t ctas = n_tiles * C;
     const int64_t waves = (ctas + slots - 1) / slots;
-    const double eff = double(ctas) / double(waves * slots);
+    const double eff = double(ctas) / double(waves * (2 * int64_t(num_sms)));
     if (eff > best + 1e-9) {
       best = eff;
       bestC = C;
@@ -384,6 +434,8 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
   p->smem_bytes = J == 1 ? Layout<1>::kSmem : Layout<2>::kSmem;
   p->reserved = static_cast<int32_t>((kbt + C - 1) / C);
 }
+
+bool decode_supported(const GemmArgs &g) { return decode_supported_impl(g); }
 
 cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
   const int J = pl.m_tile / 8;

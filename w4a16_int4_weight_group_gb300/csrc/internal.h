@@ -53,7 +53,9 @@ cudaError_t launch_gemm_generic(const GemmArgs &g);
 
 // Decode path (M <= 16): plan fields m_tile and k_split are honoured.
 bool decode_supported(const GemmArgs &g);
-void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, w4a16_plan_t *p);
+// query_device: use the runtime's occupancy queries (needs a device); otherwise assume 2 CTAs per SM.
+void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool query_device,
+                      w4a16_plan_t *p);
 cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &p);
 cudaError_t decode_take_device_error(uint32_t *err);
 cudaError_t decode_set_wait_limit_ns(uint64_t ns);
