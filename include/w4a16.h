@@ -23,7 +23,7 @@
  * Conventions shared by every entry point:
  *   - Tensor pointers are device pointers owned by the caller, contiguous and row-major. Natural
  *     alignment is required (2 bytes for 16-bit tensors, 4 bytes for int32). Higher alignment
- *     (16 bytes) and N % 32 == 0, K % 16 == 0 unlock the fast paths; otherwise a generic GPU path runs.
+ *     (16 bytes) and N % 32 == 0, K % 8 == 0 unlock the TMA-fed paths; otherwise a generic GPU path runs.
  *   - scales, bias, out and w_out have the dtype of A.
  *   - Calls are stream-ordered on `stream` (a cudaStream_t; NULL is the legacy default stream).
  *     w4a16_gemm, w4a16_pack, w4a16_unpack and w4a16_dequant allocate nothing, do not synchronise and
@@ -62,8 +62,8 @@ typedef enum {
 typedef enum {
   W4A16_PATH_NONE = 0,    /* M == 0: nothing to do                                            */
   W4A16_PATH_GENERIC = 1, /* any alignment: one thread per (8 output columns, 8 rows), K-sliced   */
-  W4A16_PATH_DECODE = 2,  /* M <= 64: split-K skinny GEMM, cp.async 16-byte streams, mma.sync,
-                             in-register magic-number dequant, cluster (DSMEM) split-K reduction */
+  W4A16_PATH_DECODE = 2,  /* M <= 16: split-K skinny GEMM, TMA weight stream, ldmatrix.trans +
+                             in-register magic-number dequant, mma.sync, cluster (DSMEM) split-K */
   W4A16_PATH_PREFILL = 3  /* large M: TMA-fed tcgen05/TMEM GEMM, int4 tiles dequantised into
                              shared memory before each UMMA                                     */
 } w4a16_path;
@@ -71,7 +71,7 @@ typedef enum {
 /* Launch plan for one w4a16_gemm call. Filled by w4a16_plan; informational. */
 typedef struct {
   int32_t path;          /* w4a16_path                                                     */
-  int32_t words_per_lane;/* DECODE: packed words per lane per row (1, 2 or 4)                 */
+  int32_t words_per_lane;/* informational (1)                                               */
   int32_t m_tile;        /* rows of A per CTA                                              */
   int32_t n_tile;        /* output columns per CTA                                         */
   int32_t k_split;       /* CTAs (one cluster) sharing one output tile along K               */
@@ -126,8 +126,8 @@ w4a16_status w4a16_dequant(const int32_t *b_q, const void *scales, const int32_t
  * Dequantised weights are rounded to the dtype before the product, exactly as w4a16_dequant returns
  * them; the sum is kept in fp32 and rounded once (nearest-even) after the bias.
  * Errors: UNSUPPORTED (dtype, group size), INVALID_ARG (shapes, nulls, zp_bias, overlap),
- *         MISALIGNED (natural alignment), CUDA (launch failure), TIMEOUT (a previous kernel of this
- *         library gave up a bounded wait; reported once, then cleared).
+ *         MISALIGNED (natural alignment), CUDA (launch failure). A kernel that gives up a bounded
+ *         device-side wait is reported later by w4a16_get_device_error (no host read happens here).
  */
 w4a16_status w4a16_gemm(const void *a, const int32_t *b_q, const void *scales, const int32_t *qzeros,
                         int group_size, int zp_bias, const void *bias, void *out, int64_t m,
@@ -167,6 +167,14 @@ int w4a16_debug_selected_path(int64_t m, int64_t k, int64_t n, int group_size);
  * the TIMEOUT status is reported without hanging the GPU. Synchronous.
  */
 w4a16_status w4a16_debug_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * w4a16_debug_inject_stall - test hook for failure detection (on != 0: enable, 0: disable). While
+ * enabled, the worker warps of the TMA-fed kernels first wait on a barrier that nothing arrives on,
+ * so that wait runs out after the bounded-wait limit: the kernel records W4A16_ERR_TIMEOUT in its
+ * device error word, releases its resources and exits without hanging. Synchronous; current device.
+ */
+w4a16_status w4a16_debug_inject_stall(int on);
 
 /* Number of kernels this library has launched in this process (all devices, all threads). */
 uint64_t w4a16_debug_launch_count(void);

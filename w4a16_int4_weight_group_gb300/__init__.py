@@ -57,6 +57,7 @@ SIGNATURES = [
     ("w4a16_get_device_error", _c_int, []),
     ("w4a16_debug_selected_path", _c_int, [_c_i64, _c_i64, _c_i64, _c_int]),
     ("w4a16_debug_set_wait_limit_ns", _c_int, [ctypes.c_uint64]),
+    ("w4a16_debug_inject_stall", _c_int, [_c_int]),
     ("w4a16_debug_launch_count", ctypes.c_uint64, []),
     ("w4a16_version", ctypes.c_char_p, []),
 ]
@@ -209,6 +210,10 @@ def w4a16_debug_set_wait_limit_ns(ns: int):
     _check(lib().w4a16_debug_set_wait_limit_ns(ns))
 
 
+def w4a16_debug_inject_stall(on: bool):
+    _check(lib().w4a16_debug_inject_stall(int(bool(on))))
+
+
 def w4a16_debug_launch_count() -> int:
     return int(lib().w4a16_debug_launch_count())
 
@@ -219,5 +224,6 @@ def w4a16_version() -> str:
 
 __all__ = ["w4a16_pack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_can_implement", "w4a16_plan",
            "w4a16_get_device_error", "w4a16_debug_selected_path", "w4a16_debug_set_wait_limit_ns",
+           "w4a16_debug_inject_stall",
            "w4a16_debug_launch_count", "w4a16_version", "W4A16Error", "lib", "last_error", "LIB_PATH",
            "SIGNATURES", "PATHS"]

@@ -364,4 +364,11 @@ w4a16_status w4a16_debug_set_wait_limit_ns(uint64_t ns) {
   return ok();
 }
 
+w4a16_status w4a16_debug_inject_stall(int on) {
+  cudaError_t e = prefill_set_stall(on != 0);
+  if (e == cudaSuccess) e = decode_set_stall(on != 0);
+  if (e != cudaSuccess) return cuda_fail(e, "set stall hook");
+  return ok();
+}
+
 }  // extern "C"

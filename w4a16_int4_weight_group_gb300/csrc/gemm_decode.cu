@@ -47,6 +47,7 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 __device__ unsigned int g_decode_error;
 __device__ unsigned long long g_decode_wait_limit_ns;
+__device__ unsigned int g_decode_stall;  // test hook: consumers first wait on a barrier nobody arrives on
 
 template <int J>
 struct Layout {
@@ -59,7 +60,7 @@ struct Layout {
   static constexpr int kOffS = kOffA + kStages * kA;
   static constexpr int kOffZ = kOffS + kStages * kS;
   static constexpr int kOffBar = kOffZ + kStages * kZ;
-  static constexpr int kOffFlag = kOffBar + 2 * kStages * 8;
+  static constexpr int kOffFlag = kOffBar + (2 * kStages + 1) * 8;  // + the stall-test barrier
   static constexpr int kUsed = kOffFlag + 16;
   static constexpr int kSmem = kUsed + 1024;    // slack to align the base to 1024 bytes
   static constexpr int kRedBytes = 8 * J * BN * 4;
@@ -132,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int nkb = min(p.kb_total, kb_begin + p.kb_per_cta) - kb_begin;
 
   const uint32_t full0 = base + L::kOffBar, empty0 = full0 + 8u * kStages;
+  const uint32_t stall_bar = empty0 + 8u * kStages;
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(base_ptr + L::kOffFlag);
   const unsigned long long lim = g_decode_wait_limit_ns;
   const uint64_t limit_ns = lim ? lim : kDefaultWaitNs;
@@ -141,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(full0 + 8u * s, 1);
       mbar_init(empty0 + 8u * s, kConsumers);
     }
+    mbar_init(stall_bar, 1);
     *abort_flag = 0u;
     mbar_init_fence();
   }
@@ -202,7 +205,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     int gpos = (kb_begin % p.spg);
     bool ok = true;
-    for (int i = 0; i < nkb; ++i) {
+    if (g_decode_stall) {  // failure-detection test: a wait that can only run out
+      ok = wait_phase(stall_bar, 0, abort_flag, limit_ns, &g_decode_error);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    for (int i = 0; i < nkb && ok; ++i) {
       const int s = i & (kStages - 1);
       ok = wait_phase(full0 + 8u * s, (i / kStages) & 1, abort_flag, limit_ns, &g_decode_error);
       ok = __all_sync(0xffffffffu, ok);
@@ -521,6 +528,11 @@ cudaError_t decode_take_device_error(uint32_t *err) {
 cudaError_t decode_set_wait_limit_ns(uint64_t ns) {
   const unsigned long long v = ns;
   return cudaMemcpyToSymbol(g_decode_wait_limit_ns, &v, sizeof(v));
+}
+
+cudaError_t decode_set_stall(bool on) {
+  const unsigned int v = on ? 1u : 0u;
+  return cudaMemcpyToSymbol(g_decode_stall, &v, sizeof(v));
 }
 
 }  // namespace w4a16

@@ -51,7 +51,7 @@ constexpr int kOffP = kOffB + SB * kBBytes;
 constexpr int kOffS = kOffP + SA * kPBytes;
 constexpr int kOffZ = kOffS + SA * kSBytes;
 constexpr int kOffBar = kOffZ + SA * kZBytes;
-constexpr int kNumBars = 2 * SA + 2 * SB + 1;
+constexpr int kNumBars = 2 * SA + 2 * SB + 2;  // + accumulator-full and the stall-test barrier
 constexpr int kOffSlot = kOffBar + kNumBars * 8;
 constexpr int kOffFlag = kOffSlot + 4;
 constexpr int kSmemUsed = kOffFlag + 4;
@@ -63,6 +63,7 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 
 __device__ unsigned int g_prefill_error;
 __device__ unsigned long long g_wait_limit_ns;
+__device__ unsigned int g_prefill_stall;  // test hook: dequantisers first wait on a barrier nobody arrives on
 
 // ---------------------------------------------------------------------------------------------
 // PTX wrappers: mbarrier, TMA, tcgen05
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto full_b = [&](int s) { return bar0 + 8u * (2 * SA + s); };
   auto empty_b = [&](int s) { return bar0 + 8u * (2 * SA + SB + s); };
   const uint32_t accum_full = bar0 + 8u * (2 * SA + 2 * SB);
+  const uint32_t stall_bar = accum_full + 8u;
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(base_ptr + kOffFlag);
   const uint32_t slot = base + kOffSlot;
 
@@ -175,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty_b(s), 1);
     }
     mbar_init(accum_full, 1);
+    mbar_init(stall_bar, 1);
     *abort_flag = 0u;
     mbar_init_fence();
   }
@@ -261,7 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         zsub[g][1] = zsub[g][3] = hi | (hi << 16);
       }
     }
-    for (int kb = 0; kb < nk; ++kb) {
+    if (g_prefill_stall) {  // failure-detection test: a wait that can only run out
+      ok = wait_phase(stall_bar, 0, abort_flag, limit_ns, &g_prefill_error);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    for (int kb = 0; kb < nk && ok; ++kb) {
       const int sa = kb % SA, sb = kb % SB;
       ok = wait_phase(full_a(sa), (kb / SA) & 1, abort_flag, limit_ns, &g_prefill_error) &&
            wait_phase(empty_b(sb), ((kb / SB) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error);
@@ -480,6 +487,11 @@ cudaError_t prefill_take_device_error(uint32_t *err) {
 cudaError_t prefill_set_wait_limit_ns(uint64_t ns) {
   const unsigned long long v = ns;
   return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof(v));
+}
+
+cudaError_t prefill_set_stall(bool on) {
+  const unsigned int v = on ? 1u : 0u;
+  return cudaMemcpyToSymbol(g_prefill_stall, &v, sizeof(v));
 }
 
 }  // namespace w4a16

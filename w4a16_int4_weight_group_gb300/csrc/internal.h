@@ -59,6 +59,7 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
 cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &p);
 cudaError_t decode_take_device_error(uint32_t *err);
 cudaError_t decode_set_wait_limit_ns(uint64_t ns);
+cudaError_t decode_set_stall(bool on);
 
 // Prefill path (tcgen05).
 bool prefill_supported(const GemmArgs &g);
@@ -67,5 +68,6 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &p);
 // Reads and clears the device error word of the prefill kernels on the current device.
 cudaError_t prefill_take_device_error(uint32_t *err);
 cudaError_t prefill_set_wait_limit_ns(uint64_t ns);
+cudaError_t prefill_set_stall(bool on);
 
 }  // namespace w4a16
