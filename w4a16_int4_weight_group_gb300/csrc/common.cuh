@@ -140,6 +140,10 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
+// Cluster barrier without memory ordering (used only to keep shared memory alive for peers).
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
 // Maps a shared::cta address of this CTA to the same offset in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
   uint32_t r;
@@ -164,17 +168,30 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_init_fence() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-// Returns true once the phase with the given parity has completed. The thread may be suspended for
-// up to `hint_ns` inside the instruction while it waits, which keeps polling off the issue slots.
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns = 1000u) {
+// Returns true once the phase with the given parity has completed (the instruction itself waits
+// for a short, hardware-defined time before reporting that it has not).
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+// A shared-memory flag read and written through the shared window (not a generic pointer).
+__device__ __forceinline__ uint32_t ld_flag(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_flag(uint32_t addr, uint32_t v) {
+  asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Fetches a TMA descriptor (a __grid_constant__ kernel parameter) ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const void *tensor_map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tensor_map)) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -196,19 +213,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tensor_map
 }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// Bounded wait on an mbarrier phase. On expiry it sets *abort_flag (shared) and ORs `code` into the
-// kernel's device error word; it also returns false early once another thread has set the flag.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+// Bounded wait on an mbarrier phase. On expiry it sets the CTA's abort flag (a shared-memory word
+// at `abort_flag`) and ORs 1 into the kernel's device error word; it also returns false early once
+// another thread has set the flag.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint32_t abort_flag,
                                            uint64_t limit_ns, unsigned int *error_word) {
-  // the suspend hint never exceeds the limit, so a short limit is honoured promptly
-  const uint32_t hint = limit_ns < 1000u ? static_cast<uint32_t>(limit_ns) : 1000u;
-  if (mbar_try_wait(bar, parity, hint)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(bar, parity, hint)) return true;
-    if (*abort_flag) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (ld_flag(abort_flag)) return false;
     if (globaltimer() - t0 > limit_ns) {
-      *abort_flag = 1u;
+      st_flag(abort_flag, 1u);
       atomicOr(error_word, 1u);
       return false;
     }

@@ -43,6 +43,7 @@ constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int BN = 256;                        // output columns per CTA
 constexpr int BK = 64;                         // rows of K per stage
 constexpr int kStages = 8;
+constexpr int kMaxCluster = 16;  // split-K factor: cluster sizes above 8 are non-portable
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 __device__ unsigned int g_decode_error;
@@ -61,10 +62,10 @@ struct Layout {
   static constexpr int kOffZ = kOffS + kStages * kS;
   static constexpr int kOffBar = kOffZ + kStages * kZ;
   static constexpr int kOffFlag = kOffBar + (2 * kStages + 1) * 8;  // + the stall-test barrier
-  static constexpr int kUsed = kOffFlag + 16;
-  static constexpr int kSmem = kUsed + 1024;    // slack to align the base to 1024 bytes
+  static constexpr int kOffRed = kOffFlag + 16;                       // split-K partial tile [8J][256]
   static constexpr int kRedBytes = 8 * J * BN * 4;
-  static_assert(kRedBytes <= kStages * kP, "reduction buffer aliases the weight stages");
+  static constexpr int kUsed = kOffRed + kRedBytes;
+  static constexpr int kSmem = kUsed + 1024;    // slack to align the base to 1024 bytes
   static_assert(kOffA % 1024 == 0 && kA % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
 
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const uint32_t full0 = base + L::kOffBar, empty0 = full0 + 8u * kStages;
   const uint32_t stall_bar = empty0 + 8u * kStages;
-  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(base_ptr + L::kOffFlag);
+  const uint32_t abort_flag = base + L::kOffFlag;
   const unsigned long long lim = g_decode_wait_limit_ns;
   const uint64_t limit_ns = lim ? lim : kDefaultWaitNs;
 
@@ -144,8 +145,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(empty0 + 8u * s, kConsumers);
     }
     mbar_init(stall_bar, 1);
-    *abort_flag = 0u;
+    st_flag(abort_flag, 0u);
     mbar_init_fence();
+  }
+  if (warp == kConsumers && lane == 0) {
+    // descriptors live in the kernel parameters, not in memory an earlier kernel writes
+    prefetch_tensormap(&tmP);
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmS);
+    if constexpr (HAS_ZP) prefetch_tensormap(&tmZ);
   }
   __syncthreads();
   // Inputs may come from the previous kernel of the stream: wait for it before the first global
@@ -179,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if constexpr (HAS_ZP) tma_load_2d(base + L::kOffZ + s * L::kZ, &tmZ, static_cast<int>(n0 / 8), grow, full);
         issued = i + 1;
       }
-      if (*abort_flag) {
+      if (ld_flag(abort_flag)) {
         for (int i = issued - 1; i >= 0 && i >= issued - kStages; --i)
           drain_phase(full0 + 8u * (i & (kStages - 1)), (i / kStages) & 1, &g_decode_error);
       }
@@ -303,8 +311,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
   } else {
-    __syncthreads();  // all stages consumed and all copies landed: the weight ring becomes red[m][n]
-    float *red = reinterpret_cast<float *>(base_ptr + L::kOffP);
+    float *red = reinterpret_cast<float *>(base_ptr + L::kOffRed);
     if (warp < kConsumers) {
       const int nl = 32 * warp + 4 * gl;
 #pragma unroll
@@ -323,21 +330,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int per = (kTile + C - 1) / C;
     const int o_begin = rank * per;
     const int o_end = o_begin + per < kTile ? o_begin + per : kTile;
-    const uint32_t red_u32 = base + L::kOffP;
+    const uint32_t red_u32 = base + L::kOffRed;
     for (int o = o_begin + threadIdx.x; o < o_end; o += kThreads) {
       const int m = o / BN;
       if (m < rows) {
         // issue every rank's load before summing (in rank order: deterministic)
-        float part[8];
+        float part[kMaxCluster];
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) part[rr] = rr < C ? ld_dsmem_f32(map_to_rank(red_u32 + 4u * o, rr)) : 0.f;
+        for (int rr = 0; rr < kMaxCluster; ++rr)
+          part[rr] = rr < C ? ld_dsmem_f32(map_to_rank(red_u32 + 4u * o, rr)) : 0.f;
         float v = 0.f;
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) v += part[rr];
+        for (int rr = 0; rr < kMaxCluster; ++rr) v += part[rr];
         finish(m, n0 + (o % BN), v);
       }
     }
-    cluster_sync_all();  // keep this CTA's shared memory alive until every rank has read it
+    cluster_sync_relaxed();  // keep this CTA's shared memory alive until every rank has read it
   }
 }
 
@@ -368,8 +376,8 @@ bool decode_supported_impl(const GemmArgs &g) {
 // (0 when unknown: no device). Queried from the runtime once per device and cluster size.
 int64_t resident_ctas(int J, int C) {
   static std::mutex mu;
-  static int cache[64][2][9];
-  static bool have[64][2][9] = {};
+  static int cache[64][2][kMaxCluster + 1];
+  static bool have[64][2][kMaxCluster + 1] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
@@ -377,7 +385,8 @@ int64_t resident_ctas(int J, int C) {
     const KernelFn fn = pick(W4A16_F16, J, true, false);
     const int smem = J == 1 ? Layout<1>::kSmem : Layout<2>::kSmem;
     int n = 0;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
+        (C <= 8 || cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess)) {
       if (C == 1) {
         int per_sm = 0, sms = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) == cudaSuccess &&
@@ -414,19 +423,22 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
   const int J = M <= 8 ? 1 : 2;
   const int64_t n_tiles = (N + BN - 1) / BN;
   const int64_t kbt = (K + BK - 1) / BK;
-  // Choose the cluster size C (split-K factor) that keeps the most CTAs busy in full waves; the
-  // resident count comes from the runtime's occupancy query (two CTAs per SM when unknown).
+  // Choose the cluster size C (split-K factor) minimising waves x per-CTA time, where a CTA costs a
+  // fixed latency (launch, first TMA round trip, cluster reduction) plus its K blocks; the number of
+  // CTAs resident at once comes from the runtime's occupancy query (two per SM when unknown).
+  constexpr double kFixedUs = 2.5, kPerBlockUs = 0.3;
   int bestC = 1;
   double best = -1.0;
-  for (int C = 1; C <= 8; ++C) {
+  for (int C = 1; C <= kMaxCluster; ++C) {
     if (C > 1 && kbt < 2 * int64_t(C)) break;  // every rank keeps at least two K blocks
     int64_t slots = query_device ? resident_ctas(J, C) : 0;
-    if (slots <= 0) slots = 2 * int64_t(num_sms) / C * C;
+    if (slots <= 0) slots = C <= 8 ? 2 * int64_t(num_sms) / C * C : 0;
+    if (slots <= 0) continue;
     const int64_t ctas = n_tiles * C;
     const int64_t waves = (ctas + slots - 1) / slots;
-    const double eff = double(ctas) / double(waves * (2 * int64_t(num_sms)));
-    if (eff > best + 1e-9) {
-      best = eff;
+    const double cost = double(waves) * (kFixedUs + kPerBlockUs * double((kbt + C - 1) / C));
+    if (best < 0 || cost < best - 1e-9) {
+      best = cost;
       bestC = C;
     }
   }
@@ -473,6 +485,8 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
     bool &done = configured[dev & 63][g.dtype == W4A16_BF16][J - 1][zp][two];
     if (!done) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
       done = true;
     }

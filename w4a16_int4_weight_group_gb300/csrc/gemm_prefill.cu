@@ -5,7 +5,8 @@
 // BLOCK_M/N/K chosen at run time, BLOCK_K clamped to the group size; PR #40977 report, key source
 // snippets: fp32 accumulator, dequantise then multiply-add per K tile). On sm_103a this becomes:
 //
-//  * CTA tile 128 (rows of A) x 256 (output columns), K in blocks of 64. One CTA per tile, 10 warps:
+//  * CTA tile 128*MT (rows of A; MT = 1 or 2 accumulators) x 256 (output columns), K in blocks of
+//    64. One CTA per tile, 10 warps:
 //      warp 0      TMA producer: A tile (128x64, 128-byte swizzle), packed weight tile (64 rows x 32
 //                  words), the one or two scale rows and zero-point rows the block needs;
 //      warp 1      TMEM allocator and the single MMA-issuing thread;
@@ -17,9 +18,11 @@
 //    the value w4a16_dequant writes. The 16-byte result (columns n, n+4, n+1, n+5, ...) goes to the
 //    shared-memory B tile in the MN-major 128-byte-swizzled layout the tensor core reads; the epilogue
 //    undoes the column interleave.
-//  * MMA: tcgen05.mma.cta_group::1.kind::f16, M=128, N=256, K=16, fp32 accumulator in 256 TMEM
-//    columns; A K-major, B MN-major. tcgen05.commit frees the shared-memory stages.
-//  * Pipelines: 4 stages of (A, packed, scales, zeros) and 3 stages of dequantised B, each with
+//  * MMA: tcgen05.mma.cta_group::1.kind::f16, M=128, N=256, K=16, one per 128-row half of the
+//    tile, fp32 accumulators in 256*MT TMEM columns; A K-major, B MN-major. Each dequantised B tile
+//    feeds MT MMAs, so MT = 2 halves the dequantisation work per FLOP. tcgen05.commit frees stages.
+//  * Pipelines: 4 (MT=1) or 3 (MT=2) stages of (A, packed, scales, zeros) and 3 stages of
+//    dequantised B, each with
 //    full/empty mbarriers. Every wait is bounded (default 2 s, settable for tests): on expiry the CTA
 //    records an error word, stops, drains its own TMA copies and MMAs with a fixed bound, frees its
 //    TMEM and exits without writing output.
@@ -33,31 +36,37 @@
 namespace w4a16 {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int SA = 4;  // stages of A / packed weights / scales / zeros
-constexpr int SB = 3;  // stages of dequantised weights
+constexpr int BN = 256, BK = 64;
 constexpr int kDequantWarps = 8;
 constexpr int kThreads = 32 * (2 + kDequantWarps);
-constexpr uint32_t kTmemCols = 256;
 
-constexpr int kABytes = BM * BK * 2;        // 16 KB
-constexpr int kPBytes = BK * (BN / 8) * 4;  // 8 KB
-constexpr int kSBytes = 2 * BN * 2;         // up to two scale rows
-constexpr int kZBytes = 2 * (BN / 8) * 4;   // up to two zero-point rows
-constexpr int kBBytes = BK * BN * 2;        // 32 KB
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + SA * kABytes;
-constexpr int kOffP = kOffB + SB * kBBytes;
-constexpr int kOffS = kOffP + SA * kPBytes;
-constexpr int kOffZ = kOffS + SA * kSBytes;
-constexpr int kOffBar = kOffZ + SA * kZBytes;
-constexpr int kNumBars = 2 * SA + 2 * SB + 2;  // + accumulator-full and the stall-test barrier
-constexpr int kOffSlot = kOffBar + kNumBars * 8;
-constexpr int kOffFlag = kOffSlot + 4;
-constexpr int kSmemUsed = kOffFlag + 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 bytes
-static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+// MT accumulators of 128 rows each: the CTA tile is 128*MT rows x 256 columns, and each
+// dequantised weight tile feeds MT MMAs.
+template <int MT>
+struct PLayout {
+  static constexpr int BM = 128 * MT;
+  static constexpr int SA = MT == 1 ? 4 : 3;  // stages of A / packed weights / scales / zeros
+  static constexpr int SB = 3;                 // stages of dequantised weights
+  static constexpr uint32_t kTmemCols = 256u * MT;
+  static constexpr int kABytes = BM * BK * 2;        // 16 KB per 128 rows
+  static constexpr int kPBytes = BK * (BN / 8) * 4;  // 8 KB
+  static constexpr int kSBytes = 2 * BN * 2;         // up to two scale rows
+  static constexpr int kZBytes = 2 * (BN / 8) * 4;   // up to two zero-point rows
+  static constexpr int kBBytes = BK * BN * 2;        // 32 KB
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + SA * kABytes;
+  static constexpr int kOffP = kOffB + SB * kBBytes;
+  static constexpr int kOffS = kOffP + SA * kPBytes;
+  static constexpr int kOffZ = kOffS + SA * kSBytes;
+  static constexpr int kOffBar = kOffZ + SA * kZBytes;
+  static constexpr int kNumBars = 2 * SA + 2 * SB + 2;  // + accumulator-full and the stall-test barrier
+  static constexpr int kOffSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffFlag = kOffSlot + 4;
+  static constexpr int kSmemUsed = kOffFlag + 4;
+  static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 bytes
+  static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
 
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 
@@ -138,12 +147,19 @@ __device__ __forceinline__ void magic4(uint32_t w, uint32_t (&h)[4]) {
   }
 }
 
-template <class DT, bool HAS_ZP, bool TWO_GROUPS>
+template <class DT, bool HAS_ZP, bool TWO_GROUPS, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmP,
                    const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ,
                    const PrefillParams p) {
   constexpr bool BF = DT::kBF16;
+  using L = PLayout<MT>;
+  constexpr int BM = L::BM, SA = L::SA, SB = L::SB;
+  constexpr int kABytes = L::kABytes, kPBytes = L::kPBytes, kSBytes = L::kSBytes, kZBytes = L::kZBytes,
+                kBBytes = L::kBBytes;
+  constexpr int kOffA = L::kOffA, kOffB = L::kOffB, kOffP = L::kOffP, kOffS = L::kOffS, kOffZ = L::kOffZ,
+                kOffBar = L::kOffBar, kOffSlot = L::kOffSlot, kOffFlag = L::kOffFlag;
+  constexpr uint32_t kTmemCols = L::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -161,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto empty_b = [&](int s) { return bar0 + 8u * (2 * SA + SB + s); };
   const uint32_t accum_full = bar0 + 8u * (2 * SA + 2 * SB);
   const uint32_t stall_bar = accum_full + 8u;
-  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(base_ptr + kOffFlag);
+  const uint32_t abort_flag = base + kOffFlag;
   const uint32_t slot = base + kOffSlot;
 
   const unsigned long long lim = g_wait_limit_ns;
@@ -178,13 +194,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(accum_full, 1);
     mbar_init(stall_bar, 1);
-    *abort_flag = 0u;
+    st_flag(abort_flag, 0u);
     mbar_init_fence();
+  }
+  if (warp == 0 && lane == 0) {
+    // descriptors live in the kernel parameters, not in memory an earlier kernel writes
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmP);
+    prefetch_tensormap(&tmS);
+    if constexpr (HAS_ZP) prefetch_tensormap(&tmZ);
   }
   if (warp == 1) tmem_alloc(slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Inputs may come from the previous kernel of the stream: wait for it before the first global
+  // access, then let the next kernel begin launching.
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(base_ptr + kOffSlot);
 
   const int nk = p.nk;
@@ -208,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (HAS_ZP) tma_load_2d(base + kOffZ + s * kZBytes, &tmZ, static_cast<int>(n0 / 8), grow, full_a(s));
         issued = kb + 1;
       }
-      if (*abort_flag) {
+      if (ld_flag(abort_flag)) {
         // let this CTA's own copies land before its shared memory is released
         for (int kb = issued - 1; kb >= 0 && kb >= issued - SA; --kb) drain_phase(full_a(kb % SA), (kb / SA) & 1, &g_prefill_error);
       }
@@ -222,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              | (0u << 15)                      // A K-major
                              | (1u << 16)                      // B MN-major
                              | (uint32_t(BN >> 3) << 17)       // N
-                             | (uint32_t(BM >> 4) << 24);      // M
+                             | (uint32_t(128 >> 4) << 24);     // M (one MMA per 128-row half)
       bool ok = true;
       for (int kb = 0; kb < nk && ok; ++kb) {
         const int sa = kb % SA, sb = kb % SB;
@@ -234,12 +261,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b_base = base + kOffB + sb * kBBytes;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; a K step of 16 is 32 bytes.
-          const uint64_t ad = smem_desc(a_base + 32u * kk, 16u, 1024u);
           // B: MN-major, 128-byte swizzle atoms of 64 columns x 8 rows; atoms along N 1024 B apart
           // (leading), 8-row K groups 4096 B apart (stride); a K step of 16 is two groups.
           const uint64_t bd = smem_desc(b_base + 8192u * kk, 1024u, 4096u);
-          umma_f16(tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; a K step of 16 is 32 bytes;
+            // rows 128*mt.. start 16 KB further. Accumulator mt lives in TMEM columns 256*mt..
+            const uint64_t ad = smem_desc(a_base + 16384u * mt + 32u * kk, 16u, 1024u);
+            umma_f16(tmem + 256u * mt, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
         }
         umma_commit(empty_a(sa));
         umma_commit(empty_b(sb));
@@ -322,14 +353,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                // TMEM lane quarter this warp may read
     const int row = 32 * q + lane;
     const int half = dw >> 2;              // columns [128*half, 128*half + 128)
-    const int64_t m = m0 + row;
-    const bool row_ok = m < p.M;
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
+    for (int it = 0; it < 4 * MT; ++it) {
+      const int mt = it >> 2, ch = it & 3;  // accumulator (row half of the tile) and 32-column chunk
+      const int64_t m = m0 + 128 * mt + row;
+      const bool row_ok = m < p.M;
       const int col0 = half * 128 + ch * 32;
       uint32_t r[32];
       if (ok) {
-        tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(col0), r);
+        tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(256 * mt + col0), r);
         tmem_wait_ld();
       }
       if (ok && row_ok) {
@@ -390,14 +422,16 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                           const PrefillParams);
 
-template <class DT>
+template <class DT, int MT>
 KernelFn pick_dt(bool zp, bool two) {
-  if (zp) return two ? prefill_kernel<DT, true, true> : prefill_kernel<DT, true, false>;
-  return two ? prefill_kernel<DT, false, true> : prefill_kernel<DT, false, false>;
+  if (zp) return two ? prefill_kernel<DT, true, true, MT> : prefill_kernel<DT, true, false, MT>;
+  return two ? prefill_kernel<DT, false, true, MT> : prefill_kernel<DT, false, false, MT>;
 }
-KernelFn pick(int dtype, bool zp, bool two) {
-  return dtype == W4A16_BF16 ? pick_dt<BF16>(zp, two) : pick_dt<F16>(zp, two);
+KernelFn pick(int dtype, bool zp, bool two, int MT) {
+  if (dtype == W4A16_BF16) return MT == 2 ? pick_dt<BF16, 2>(zp, two) : pick_dt<BF16, 1>(zp, two);
+  return MT == 2 ? pick_dt<F16, 2>(zp, two) : pick_dt<F16, 1>(zp, two);
 }
+int smem_of(int MT) { return MT == 2 ? PLayout<2>::kSmemBytes : PLayout<1>::kSmemBytes; }
 
 }  // namespace
 
@@ -410,19 +444,33 @@ bool prefill_supported(const GemmArgs &g) {
 void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, w4a16_plan_t *p) {
   (void)K;
   (void)group_size;
-  (void)num_sms;
+  // One CTA per SM (shared memory). Two 128-row accumulators halve the dequantisation work per
+  // FLOP; use them unless the doubled tile costs more waves x work than single ones.
+  const int64_t n_tiles = (N + BN - 1) / BN;
+  int64_t best_cost = -1;
+  int MT = 1;
+  for (int mt = 2; mt >= 1; --mt) {
+    const int64_t tiles = ((M + 128 * mt - 1) / (128 * mt)) * n_tiles;
+    const int64_t cost = ((tiles + num_sms - 1) / num_sms) * mt;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      MT = mt;
+    }
+  }
   p->path = W4A16_PATH_PREFILL;
   p->words_per_lane = 1;
-  p->m_tile = BM;
+  p->m_tile = 128 * MT;
   p->n_tile = BN;
   p->k_split = 1;
   p->warps = kThreads / 32;
-  p->grid = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  p->smem_bytes = kSmemBytes;
+  p->grid = ((M + 128 * MT - 1) / (128 * MT)) * n_tiles;
+  p->smem_bytes = smem_of(MT);
   p->reserved = 0;
 }
 
-cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &) {
+cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl) {
+  const int MT = pl.m_tile / 128;
+  const int BM = 128 * MT;
   const bool zp = g.qzeros != nullptr;
   const int64_t NW = g.N / 8, ng = g.K / g.group_size;
   const bool two = g.group_size < BK && g.group_size != g.K;  // G = 32: two groups per K block
@@ -437,17 +485,17 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &) {
   } else {
     tZ = tP;  // unused
   }
-  const KernelFn fn = pick(g.dtype, zp, two);
+  const KernelFn fn = pick(g.dtype, zp, two, MT);
   {
     static std::mutex mu;
-    static bool configured[64][2][2][2] = {};
+    static bool configured[64][2][2][2][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
-    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][zp][two];
+    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][zp][two][MT - 1];
     if (!done) {
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_of(MT));
       if (e != cudaSuccess) return e;
       done = true;
     }
@@ -465,10 +513,13 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((g.M + BM - 1) / BM), static_cast<unsigned>((g.N + BN - 1) / BN), 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_of(MT);
   cfg.stream = g.stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tA, tP, tS, tZ, prm);
   if (e != cudaSuccess) return e;
   note_launch();
