@@ -28,6 +28,12 @@
  *   - Calls are stream-ordered on `stream` (a cudaStream_t; NULL is the legacy default stream).
  *     w4a16_gemm, w4a16_pack, w4a16_unpack and w4a16_dequant allocate nothing, do not synchronise and
  *     read nothing back to the host, and keep no pointer after they return.
+ *   - w4a16_gemm kernels use programmatic dependent launch: when the previous kernel of the stream
+ *     releases its dependents early (as this library's kernels do), a w4a16_gemm kernel may start
+ *     fetching b_q, scales and qzeros - model parameters - before that kernel has finished. a and bias
+ *     are read, and out is written, only after it has completed. So do not let the kernel that runs
+ *     just before w4a16_gemm on the same stream write that call's b_q, scales or qzeros unless it
+ *     completes normally (kernels that do not use programmatic launch always do).
  *   - Errors are reported by the returned status; a human-readable reason for the last failure on the
  *     calling thread is available from w4a16_last_error(). Validation happens before any launch, so a
  *     rejected call touches no memory. The library never aborts the process and device code never traps.

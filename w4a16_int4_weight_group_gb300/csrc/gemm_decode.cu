@@ -38,11 +38,13 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kConsumers = 8;                  // one per 32-column block
+constexpr int kBlocksPerRow = 8;               // 32-column blocks of a 256-column tile
+constexpr int kGroups = 2;                     // consumer groups taking alternate K blocks
+constexpr int kConsumers = kBlocksPerRow * kGroups;
 constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int BN = 256;                        // output columns per CTA
 constexpr int BK = 64;                         // rows of K per stage
-constexpr int kStages = 8;
+constexpr int kStages = 16;
 constexpr int kMaxCluster = 16;  // split-K factor: cluster sizes above 8 are non-portable
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
@@ -64,7 +66,8 @@ struct Layout {
   static constexpr int kOffFlag = kOffBar + (2 * kStages + 1) * 8;  // + the stall-test barrier
   static constexpr int kOffRed = kOffFlag + 16;                       // split-K partial tile [8J][256]
   static constexpr int kRedBytes = 8 * J * BN * 4;
-  static constexpr int kUsed = kOffRed + kRedBytes;
+  static constexpr int kOffGRed = kOffRed + kRedBytes;                // second group's partial tile
+  static constexpr int kUsed = kOffGRed + kRedBytes;
   static constexpr int kSmem = kUsed + 1024;    // slack to align the base to 1024 bytes
   static_assert(kOffA % 1024 == 0 && kA % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
@@ -110,7 +113,7 @@ __device__ __forceinline__ void magic_quad(uint32_t w, uint32_t (&h)[4]) {
 }
 
 template <class DT, int J, bool HAS_ZP, bool TWO_GROUPS>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmP,
                   const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ,
                   const DecodeParams p) {
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, kConsumers);
+      mbar_init(empty0 + 8u * s, kBlocksPerRow);  // one consumer group reads each stage
     }
     mbar_init(stall_bar, 1);
     st_flag(abort_flag, 0u);
@@ -156,9 +159,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     if constexpr (HAS_ZP) prefetch_tensormap(&tmZ);
   }
   __syncthreads();
-  // Inputs may come from the previous kernel of the stream: wait for it before the first global
-  // access, then let the next kernel begin launching.
-  griddep_wait();
+  // Let the next kernel of the stream begin launching (it waits for this one before touching its
+  // own inputs). Everything this kernel reads except the weights may come from the previous kernel.
   griddep_launch_dependents();
 
   float acc[J][2][4];
@@ -173,28 +175,48 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint32_t tx = L::kP + L::kA + kSRows * BN * 2 + (HAS_ZP ? kSRows * BN / 2 : 0);
-      int issued = 0;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i & (kStages - 1);
-        if (!wait_phase(empty0 + 8u * s, ((i / kStages) & 1) ^ 1u, abort_flag, limit_ns, &g_decode_error)) break;
+      auto load_weights = [&](int i, int s) {
         const uint32_t full = full0 + 8u * s;
-        mbar_arrive_expect_tx(full, tx);
         const int k0 = (kb_begin + i) * BK;
         const int grow = k0 / p.G;
         tma_load_2d(base + L::kOffP + s * L::kP, &tmP, static_cast<int>(n0 / 8), k0, full);
-        tma_load_2d(base + L::kOffA + s * L::kA, &tmA, k0, 0, full);
         tma_load_2d(base + L::kOffS + s * L::kS, &tmS, static_cast<int>(n0), grow, full);
         if constexpr (HAS_ZP) tma_load_2d(base + L::kOffZ + s * L::kZ, &tmZ, static_cast<int>(n0 / 8), grow, full);
+      };
+      auto load_acts = [&](int i, int s) {
+        tma_load_2d(base + L::kOffA + s * L::kA, &tmA, (kb_begin + i) * BK, 0, full0 + 8u * s);
+      };
+      // The packed weights, scales and zero points are model parameters that no kernel of this stream
+      // writes while it runs: the first ring of them is requested before waiting for the previous
+      // kernel, which overlaps their latency with its tail. The activations come after the wait.
+      const int first = nkb < kStages ? nkb : kStages;
+      for (int i = 0; i < first; ++i) {
+        mbar_arrive_expect_tx(full0 + 8u * i, tx);
+        load_weights(i, i);
+      }
+      griddep_wait();
+      for (int i = 0; i < first; ++i) load_acts(i, i);
+      int issued = first;
+      for (int i = first; i < nkb; ++i) {
+        const int s = i & (kStages - 1);
+        if (!wait_phase(empty0 + 8u * s, ((i / kStages) & 1) ^ 1u, abort_flag, limit_ns, &g_decode_error)) break;
+        mbar_arrive_expect_tx(full0 + 8u * s, tx);
+        load_weights(i, s);
+        load_acts(i, s);
         issued = i + 1;
       }
       if (ld_flag(abort_flag)) {
         for (int i = issued - 1; i >= 0 && i >= issued - kStages; --i)
           drain_phase(full0 + 8u * (i & (kStages - 1)), (i / kStages) & 1, &g_decode_error);
       }
+    } else {
+      griddep_wait();
     }
   } else {
     // ------------------------------------------------------------------ consumers
-    const int cb = warp;  // 16-byte chunk (32 columns) of every 128-byte packed row
+    griddep_wait();  // the epilogue writes `out` and reads `bias`: the previous kernel must be done
+    const int grp = warp / kBlocksPerRow;  // K blocks grp, grp+2, grp+4, ...
+    const int cb = warp % kBlocksPerRow;   // 16-byte chunk (32 columns) of every 128-byte packed row
     // ldmatrix row addresses: lanes 8i..8i+7 -> matrix i, row (lane & 7)
     const int mi = lane >> 3, rj = lane & 7;
     const uint32_t p_off = uint32_t((8 * mi + rj) * 128 + ((cb ^ rj) << 4));          // row blocks 0..3
@@ -211,20 +233,20 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int j = 0; j < 4; ++j) zsub[g][j] = zsub_of<BF>(j, static_cast<uint32_t>(p.zp_bias));
     }
-    int gpos = (kb_begin % p.spg);
     bool ok = true;
     if (g_decode_stall) {  // failure-detection test: a wait that can only run out
       ok = wait_phase(stall_bar, 0, abort_flag, limit_ns, &g_decode_error);
       ok = __all_sync(0xffffffffu, ok);
     }
-    for (int i = 0; i < nkb && ok; ++i) {
+    for (int i = grp; i < nkb && ok; i += kGroups) {
       const int s = i & (kStages - 1);
       ok = wait_phase(full0 + 8u * s, (i / kStages) & 1, abort_flag, limit_ns, &g_decode_error);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       const uint32_t P = base + L::kOffP + s * L::kP;
       const uint32_t A = base + L::kOffA + s * L::kA;
-      if (i == 0 || gpos == 0) {
+      // this group last saw K block kb - 2: reload the scale row when a group boundary lies between
+      if (i < kGroups || (kb_begin + i) % p.spg < kGroups) {
         const uint32_t S = base + L::kOffS + s * L::kS;
 #pragma unroll
         for (int g = 0; g < kSRows; ++g) {
@@ -242,7 +264,6 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
       }
-      if (++gpos == p.spg) gpos = 0;
 
       uint32_t wq[8];        // row blocks 0..7 of column block cb
       uint32_t af[J][8];     // B fragments: (b0, b1) for k16 steps 0..3
@@ -288,6 +309,36 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // ------------------------------------------------------------------ reduction and epilogue
+  // group 1 hands its partial sums to group 0 (fixed order: group 0 + group 1)
+  {
+    float *gred = reinterpret_cast<float *>(base_ptr + L::kOffGRed);
+    const int nl = 32 * (warp % kBlocksPerRow) + 4 * gl;
+    if (warp >= kBlocksPerRow && warp < kConsumers) {
+#pragma unroll
+      for (int jt = 0; jt < J; ++jt)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int m = 8 * jt + 2 * tig;
+          gred[m * BN + nl + q] = acc[jt][q][0];
+          gred[(m + 1) * BN + nl + q] = acc[jt][q][1];
+          gred[m * BN + nl + q + 2] = acc[jt][q][2];
+          gred[(m + 1) * BN + nl + q + 2] = acc[jt][q][3];
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");  // consumer warps only
+    if (warp < kBlocksPerRow) {
+#pragma unroll
+      for (int jt = 0; jt < J; ++jt)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int m = 8 * jt + 2 * tig;
+          acc[jt][q][0] += gred[m * BN + nl + q];
+          acc[jt][q][1] += gred[(m + 1) * BN + nl + q];
+          acc[jt][q][2] += gred[m * BN + nl + q + 2];
+          acc[jt][q][3] += gred[(m + 1) * BN + nl + q + 2];
+        }
+    }
+  }
   const int64_t rows = p.M < 8 * J ? p.M : 8 * J;
   auto finish = [&](int m, int64_t n, float v) {
     if (m < rows && n < p.N) {
@@ -297,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   };
   if (C == 1) {
-    if (warp < kConsumers) {
+    if (warp < kBlocksPerRow) {
       const int64_t nb = n0 + 32 * warp + 4 * gl;
 #pragma unroll
       for (int jt = 0; jt < J; ++jt)
@@ -312,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else {
     float *red = reinterpret_cast<float *>(base_ptr + L::kOffRed);
-    if (warp < kConsumers) {
+    if (warp < kBlocksPerRow) {
       const int nl = 32 * warp + 4 * gl;
 #pragma unroll
       for (int jt = 0; jt < J; ++jt)
@@ -425,14 +476,14 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
   const int64_t kbt = (K + BK - 1) / BK;
   // Choose the cluster size C (split-K factor) minimising waves x per-CTA time, where a CTA costs a
   // fixed latency (launch, first TMA round trip, cluster reduction) plus its K blocks; the number of
-  // CTAs resident at once comes from the runtime's occupancy query (two per SM when unknown).
-  constexpr double kFixedUs = 2.5, kPerBlockUs = 0.3;
+  // CTAs resident at once comes from the runtime's occupancy query (one per SM when unknown).
+  constexpr double kFixedUs = 2.5, kPerBlockUs = 0.2;
   int bestC = 1;
   double best = -1.0;
   for (int C = 1; C <= kMaxCluster; ++C) {
     if (C > 1 && kbt < 2 * int64_t(C)) break;  // every rank keeps at least two K blocks
     int64_t slots = query_device ? resident_ctas(J, C) : 0;
-    if (slots <= 0) slots = C <= 8 ? 2 * int64_t(num_sms) / C * C : 0;
+    if (slots <= 0) slots = C <= 8 ? int64_t(num_sms) / C * C : 0;
     if (slots <= 0) continue;
     const int64_t ctas = n_tiles * C;
     const int64_t waves = (ctas + slots - 1) / slots;

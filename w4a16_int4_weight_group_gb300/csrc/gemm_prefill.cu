@@ -445,14 +445,14 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
   (void)K;
   (void)group_size;
   // One CTA per SM (shared memory). Two 128-row accumulators halve the dequantisation work per
-  // FLOP; use them unless the doubled tile costs more waves x work than single ones.
+  // FLOP, which makes a tile-row about 1.4x cheaper (measured); pick the smaller waves x work.
   const int64_t n_tiles = (N + BN - 1) / BN;
-  int64_t best_cost = -1;
+  double best_cost = -1.0;
   int MT = 1;
   for (int mt = 2; mt >= 1; --mt) {
     const int64_t tiles = ((M + 128 * mt - 1) / (128 * mt)) * n_tiles;
-    const int64_t cost = ((tiles + num_sms - 1) / num_sms) * mt;
-    if (best_cost < 0 || cost < best_cost) {
+    const double cost = double((tiles + num_sms - 1) / num_sms) * mt * (mt == 1 ? 1.4 : 1.0);
+    if (best_cost < 0 || cost < best_cost - 1e-9) {
       best_cost = cost;
       MT = mt;
     }
