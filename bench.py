@@ -195,6 +195,8 @@ def run_cuda(args, rank, world, local_rank):
 
     name = args.config
     cases = cases_of(name)
+    if args.case is not None:
+        cases = [cases[args.case]]  # one case of the workload (for profiler captures)
     unit, bound = unit_of(name)
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16}
 
@@ -222,31 +224,44 @@ def run_cuda(args, rank, world, local_rank):
                       "scales": [sc] + [sc.clone() for _ in range(reps - 1)],
                       "qzeros": None if qz is None else [qz] + [qz.clone() for _ in range(reps - 1)],
                       "bias": bi, "reps": reps, "G": G}
+    # Activations and outputs of all the calls of a step live in one device buffer each (16-byte
+    # aligned slices), mirrored by one pinned host buffer each: the end-to-end leg moves a step's
+    # inputs with one host-to-device copy and its results with one device-to-host copy.
+    a_elems = [((M * K + 7) // 8) * 8 for (M, K, *_r) in cases]
+    o_elems = [((M * N + 7) // 8) * 8 for (M, K, N, *_r) in cases]
+    edt = tdt[cases[0][4]]
+    a_dev = torch.empty(sum(a_elems), dtype=edt, device=dev)
+    o_dev = torch.empty(sum(o_elems), dtype=edt, device=dev)
+    a_pin = torch.empty(sum(a_elems), dtype=edt).pin_memory()
+    o_pin = torch.empty(sum(o_elems), dtype=edt).pin_memory()
     calls = []
+    ao = oo = 0
     for i, (M, K, N, G, dt, asym, bias, lo, hi, seed) in enumerate(cases):
         key = (K, N, G, dt, asym, bias)
-        a_host = synth.activations(M, K, dt, seed=1000 + seed)
-        a = to_t(a_host, dt).to(dev)
-        out = torch.empty((M, N), dtype=tdt[dt], device=dev)
-        calls.append({"key": key, "a": a, "a_host": to_t(a_host, dt).pin_memory(), "out": out,
-                      "out_host": torch.empty((M, N), dtype=tdt[dt]).pin_memory(),
-                      "units": units_per_case(name, (M, K, N, G, dt, asym, bias)),
+        a_host = to_t(synth.activations(M, K, dt, seed=1000 + seed), dt)
+        a_pin[ao:ao + M * K].copy_(a_host.reshape(-1))
+        a = a_dev[ao:ao + M * K].view(M, K)
+        a.copy_(a_host)
+        out = o_dev[oo:oo + M * N].view(M, N)
+        calls.append({"key": key, "a": a, "out": out, "units": units_per_case(name, (M, K, N, G, dt, asym, bias)),
                       "M": M, "K": K, "N": N})
+        ao += a_elems[i]
+        oo += o_elems[i]
     counters = {key: 0 for key in pools}
     stream = torch.cuda.Stream(dev)
 
     def one_step(use_host=False):
+        if use_host:
+            a_dev.copy_(a_pin, non_blocking=True)
         for c in calls:
             pool = pools[c["key"]]
             r = counters[c["key"]] % pool["reps"]
             counters[c["key"]] += 1
-            if use_host:
-                c["a"].copy_(c["a_host"], non_blocking=True)
             w4.w4a16_gemm(c["a"], pool["b_q"][r], pool["scales"][r],
                           None if pool["qzeros"] is None else pool["qzeros"][r], pool["G"], 8, pool["bias"],
                           out=c["out"])
-            if use_host:
-                c["out_host"].copy_(c["out"], non_blocking=True)
+        if use_host:
+            o_pin.copy_(o_dev, non_blocking=True)
 
     def barrier():
         if world > 1:
@@ -323,8 +338,8 @@ def run_cuda(args, rank, world, local_rank):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
     e2e_value = scale_units(name, units_per_step * e2e_steps * world) / (e2e_ms / 1e3)
-    h2d = sum(c["a"].numel() * c["a"].element_size() for c in calls)
-    d2h = sum(c["out"].numel() * c["out"].element_size() for c in calls)
+    h2d = a_dev.numel() * a_dev.element_size()
+    d2h = o_dev.numel() * o_dev.element_size()
 
     if rank != 0:
         return None
@@ -353,7 +368,9 @@ def run_cuda(args, rank, world, local_rank):
         "gpu_launches": launches,
         "clocks": clk,
     }
-    if not args.no_cpu_baseline and world == 1:
+    if args.case is not None:
+        line["config"]["case"] = args.case
+    if not args.no_cpu_baseline and world == 1 and args.case is None:
         line["cpu_baseline"] = cpu_baseline(name, cases, budget_s=args.cpu_seconds)
     return line
 
@@ -449,6 +466,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline budget")
     ap.add_argument("--ref-seconds", type=float, default=120.0, help="reference-arm budget for all steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", type=int, default=None, help="run only this case of the workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -84,7 +84,7 @@ typedef struct {
   int32_t warps;         /* warps per CTA                                                  */
   int64_t grid;          /* CTAs launched                                                  */
   int32_t smem_bytes;    /* dynamic shared memory per CTA                                  */
-  int32_t reserved;
+  int32_t stream_k;      /* PREFILL: 1 when persistent CTAs share (tile, K block) units evenly  */
 } w4a16_plan_t;
 
 /*
@@ -140,6 +140,27 @@ w4a16_status w4a16_gemm(const void *a, const int32_t *b_q, const void *scales, c
                         int64_t k, int64_t n, w4a16_dtype dtype, w4a16_stream_t stream);
 
 /*
+ * w4a16_gemm_ws - w4a16_gemm with a caller-owned scratch buffer, which lets large-M calls whose
+ * output tiles do not fill the GPU in whole waves use stream-K: persistent CTAs take equal shares of
+ * the (tile, K block) work and exchange fp32 partial tiles through the workspace.
+ *   workspace       device memory, 256-byte aligned, at least w4a16_gemm_workspace_size(...) bytes
+ *                   (a smaller or NULL workspace simply disables stream-K); it must be zero-filled
+ *                   before its first use, and every call leaves it zero-filled again
+ *   workspace_bytes its size
+ * Calls that may run concurrently (different streams) need different workspaces. Everything else
+ * is as for w4a16_gemm (no allocation, no synchronisation, no host read).
+ * Errors: as w4a16_gemm, plus INVALID_ARG if the workspace overlaps a tensor argument and
+ * MISALIGNED if it is not 256-byte aligned.
+ */
+w4a16_status w4a16_gemm_ws(const void *a, const int32_t *b_q, const void *scales, const int32_t *qzeros,
+                           int group_size, int zp_bias, const void *bias, void *out, int64_t m, int64_t k,
+                           int64_t n, w4a16_dtype dtype, void *workspace, size_t workspace_bytes,
+                           w4a16_stream_t stream);
+
+/* Bytes of workspace w4a16_gemm_ws can use for these sizes on the current device (0: none). */
+size_t w4a16_gemm_workspace_size(int64_t m, int64_t k, int64_t n, int group_size, int dtype);
+
+/*
  * w4a16_can_implement - host-only check of a layer configuration, mirroring
  * TritonW4A16LinearKernel.can_implement (PR #43731 report, key source snippets): returns W4A16_OK or
  * the rejection status, with the reason available from w4a16_last_error(). No device access.
@@ -148,11 +169,12 @@ w4a16_status w4a16_gemm(const void *a, const int32_t *b_q, const void *scales, c
 w4a16_status w4a16_can_implement(int64_t k, int64_t n, int group_size, int dtype, int has_g_idx);
 
 /*
- * w4a16_plan - host-only: the launch plan w4a16_gemm would use for these sizes on a device with
- * `num_sms` SMs (num_sms <= 0: query the current device). Pointer alignment is assumed to be 16 bytes.
+ * w4a16_plan - host-only: the launch plan w4a16_gemm (with_workspace == 0) or w4a16_gemm_ws with a
+ * large enough workspace (with_workspace != 0) would use for these sizes on a device with `num_sms`
+ * SMs (num_sms <= 0: query the current device). Pointer alignment is assumed to be 16 bytes.
  */
 w4a16_status w4a16_plan(int64_t m, int64_t k, int64_t n, int group_size, int dtype, int has_zp,
-                        int num_sms, w4a16_plan_t *plan);
+                        int num_sms, int with_workspace, w4a16_plan_t *plan);
 
 /* Thread-local, NUL-terminated reason for the last failing call on this thread ("" if none). */
 const char *w4a16_last_error(void);

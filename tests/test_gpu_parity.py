@@ -217,3 +217,36 @@ def test_sweep_shapes_sampled(w, M, K, N, G):
         rng = np.random.default_rng(M)
         rows = sorted({0, M - 1} | set(rng.integers(0, M, size=4).tolist()))
         check_against_oracle(c, out, rows=rows, cols=sample_cols(N, rng, k=256), label=f"{dt} {asym}")
+
+
+@pytest.mark.parametrize("M,K,N,G,dt,asym", [(512, 4096, 1024, 128, "bf16", True), (300, 2048, 768, 64, "f16", False),
+                                           (1024, 17408, 5120, 64, "bf16", True), (129, 1024, 4096, 32, "bf16", True)])
+def test_stream_k_matches_oracle_and_leaves_workspace_clean(w, M, K, N, G, dt, asym):
+    """Persistent stream-K prefill: many CTAs share each output tile through the workspace."""
+    c = synth.make_case(M, K, N, G, dt, asym=asym, bias=True, seed=M + K)
+    code = 1 if dt == "bf16" else 0
+    plan = w.w4a16_plan(M, K, N, G, code, asym, 0, with_workspace=True)
+    assert plan["path_name"] == "prefill" and plan["stream_k"] == 1, plan
+    t = case_tensors(c)
+    need = w.w4a16_gemm_workspace_size(M, K, N, G, code)
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        out = torch.empty((M, N), dtype=t["a"].dtype, device="cuda")
+        st = w.lib().w4a16_gemm_ws(*[w._ptr(x) for x in (t["a"], t["b_q"], t["scales"], t["qzeros"])], G, 8,
+                                   w._ptr(t["bias"]), w._ptr(out), M, K, N, code, w._ptr(ws), need, None)
+        assert st == 0, w.last_error()
+        torch.cuda.synchronize()
+        outs.append(torch_to_bits(out))
+    assert np.array_equal(outs[0], outs[1]), "stream-K must be deterministic"
+    grid = plan["grid"]
+    flags = ws[grid * plan["m_tile"] * 256 * 4: grid * plan["m_tile"] * 256 * 4 + grid * 4]
+    assert int(flags.count_nonzero()) == 0, "flags must be left zero"
+    rng = np.random.default_rng(M)
+    rows = sorted({0, M - 1} | set(rng.integers(0, M, size=6).tolist()))
+    check_against_oracle(c, outs[0], rows=rows, cols=sample_cols(N, rng, k=256), label="stream-K")
+    # the same call without a workspace (whole tiles per CTA) agrees within the tolerance too
+    out2 = w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"], use_workspace=False)
+    torch.cuda.synchronize()
+    check_against_oracle(c, torch_to_bits(out2), rows=rows, cols=sample_cols(N, rng, k=256), label="no workspace")

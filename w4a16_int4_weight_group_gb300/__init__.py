@@ -34,7 +34,7 @@ class W4A16Error(RuntimeError):
 class Plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("words_per_lane", ctypes.c_int32), ("m_tile", ctypes.c_int32),
                 ("n_tile", ctypes.c_int32), ("k_split", ctypes.c_int32), ("warps", ctypes.c_int32),
-                ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int32), ("stream_k", ctypes.c_int32)]
 
     def as_dict(self):
         d = {f: getattr(self, f) for f, _ in self._fields_}
@@ -51,8 +51,11 @@ SIGNATURES = [
     ("w4a16_unpack", _c_int, [_vp, _vp, _c_i64, _c_i64, _vp]),
     ("w4a16_dequant", _c_int, [_vp, _vp, _vp, _c_i64, _c_i64, _c_int, _c_int, _c_int, _vp, _vp]),
     ("w4a16_gemm", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_int, _vp]),
+    ("w4a16_gemm_ws", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_int, _vp,
+                               ctypes.c_size_t, _vp]),
+    ("w4a16_gemm_workspace_size", ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_int, _c_int]),
     ("w4a16_can_implement", _c_int, [_c_i64, _c_i64, _c_int, _c_int, _c_int]),
-    ("w4a16_plan", _c_int, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(Plan)]),
+    ("w4a16_plan", _c_int, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(Plan)]),
     ("w4a16_last_error", ctypes.c_char_p, []),
     ("w4a16_get_device_error", _c_int, []),
     ("w4a16_debug_selected_path", _c_int, [_c_i64, _c_i64, _c_i64, _c_int]),
@@ -158,12 +161,30 @@ def w4a16_dequant(b_q: torch.Tensor, scales: torch.Tensor, qzeros: Optional[torc
     return w_out
 
 
+_workspaces = {}
+
+
+def workspace_for(device: torch.device, stream, nbytes: int) -> torch.Tensor:
+    """A zero-filled scratch buffer of at least nbytes, kept per (device, stream) and grown on demand.
+
+    The library leaves it zero-filled after every call, so it is zeroed only when (re)allocated.
+    """
+    key = (device.index, int(stream))
+    buf = _workspaces.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[key] = buf
+    return buf
+
+
 def w4a16_gemm(a: torch.Tensor, b_q: torch.Tensor, scales: torch.Tensor, qzeros: Optional[torch.Tensor],
                group_size: int, zp_bias: int = 8, bias: Optional[torch.Tensor] = None,
-               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+               out: Optional[torch.Tensor] = None, use_workspace: bool = True) -> torch.Tensor:
     """out[M, N] = cast(a[M, K] @ dequant(b_q, scales, qzeros|zp_bias) + bias), fp32 accumulation.
 
     Output shape (M, b_q.shape[1] * 8), dtype and device of ``a`` (PR #51453 report, fake impl).
+    With ``use_workspace`` a per-(device, stream) scratch buffer is passed to ``w4a16_gemm_ws`` so
+    that large-M shapes can use stream-K; otherwise ``w4a16_gemm`` (no scratch) is called.
     """
     if a.dim() != 2 or b_q.dim() != 2:
         raise ValueError("a and b_q must be 2-D")
@@ -178,8 +199,16 @@ def w4a16_gemm(a: torch.Tensor, b_q: torch.Tensor, scales: torch.Tensor, qzeros:
         raise ValueError("scales, bias and out must have the dtype of a")
     if b_q.dtype != torch.int32 or (qzeros is not None and qzeros.dtype != torch.int32):
         raise ValueError("b_q and qzeros must be int32")
-    _check(lib().w4a16_gemm(_ptr(a), _ptr(b_q), _ptr(scales), _ptr(qzeros), group_size, zp_bias, _ptr(bias),
-                            _ptr(out), m, k, n, _dtype_code(a.dtype), _stream(dev)))
+    stream = _stream(dev)
+    need = int(lib().w4a16_gemm_workspace_size(m, k, n, group_size, _dtype_code(a.dtype))) if use_workspace else 0
+    if need:
+        ws = workspace_for(dev, stream.value or 0, need)
+        _check(lib().w4a16_gemm_ws(_ptr(a), _ptr(b_q), _ptr(scales), _ptr(qzeros), group_size, zp_bias,
+                                   _ptr(bias), _ptr(out), m, k, n, _dtype_code(a.dtype), _ptr(ws), ws.numel(),
+                                   stream))
+    else:
+        _check(lib().w4a16_gemm(_ptr(a), _ptr(b_q), _ptr(scales), _ptr(qzeros), group_size, zp_bias, _ptr(bias),
+                                _ptr(out), m, k, n, _dtype_code(a.dtype), stream))
     return out
 
 
@@ -191,11 +220,17 @@ def w4a16_can_implement(k: int, n: int, group_size: int, dtype, has_g_idx: bool 
 
 
 def w4a16_plan(m: int, k: int, n: int, group_size: int, dtype=W4A16_F16, has_zp: bool = False,
-               num_sms: int = 0) -> dict:
+               num_sms: int = 0, with_workspace: bool = True) -> dict:
     p = Plan()
     code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
-    _check(lib().w4a16_plan(m, k, n, group_size, code, int(bool(has_zp)), num_sms, ctypes.byref(p)))
+    _check(lib().w4a16_plan(m, k, n, group_size, code, int(bool(has_zp)), num_sms, int(bool(with_workspace)),
+                            ctypes.byref(p)))
     return p.as_dict()
+
+
+def w4a16_gemm_workspace_size(m: int, k: int, n: int, group_size: int, dtype=W4A16_F16) -> int:
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    return int(lib().w4a16_gemm_workspace_size(m, k, n, group_size, code))
 
 
 def w4a16_get_device_error() -> int:
@@ -223,6 +258,7 @@ def w4a16_version() -> str:
 
 
 __all__ = ["w4a16_pack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_can_implement", "w4a16_plan",
+           "w4a16_gemm_workspace_size", "workspace_for",
            "w4a16_get_device_error", "w4a16_debug_selected_path", "w4a16_debug_set_wait_limit_ns",
            "w4a16_debug_inject_stall",
            "w4a16_debug_launch_count", "w4a16_version", "W4A16Error", "lib", "last_error", "LIB_PATH",

@@ -90,7 +90,7 @@ int forced_path() {
 constexpr int64_t kPrefillMinM = 65;
 
 // `tma` tells whether the driver's tensor-map encoder is available (the TMA-fed paths need it).
-void choose_plan(const GemmArgs &g, int num_sms, bool tma, bool query_device, w4a16_plan_t *p) {
+void choose_plan(const GemmArgs &g, int num_sms, bool tma, bool query_device, bool workspace, w4a16_plan_t *p) {
   std::memset(p, 0, sizeof(*p));
   if (g.M == 0) {
     p->path = W4A16_PATH_NONE;
@@ -116,7 +116,7 @@ void choose_plan(const GemmArgs &g, int num_sms, bool tma, bool query_device, w4
   if (path == W4A16_PATH_DECODE) {
     decode_make_plan(g.M, g.K, g.N, g.group_size, num_sms, query_device, p);
   } else if (path == W4A16_PATH_PREFILL) {
-    prefill_make_plan(g.M, g.K, g.N, g.group_size, num_sms, p);
+    prefill_make_plan(g.M, g.K, g.N, g.group_size, num_sms, workspace, p);
   } else {
     p->path = W4A16_PATH_GENERIC;
     p->m_tile = 8;
@@ -293,19 +293,22 @@ static w4a16_status validate_gemm(const GemmArgs &g) {
   return W4A16_OK;
 }
 
-w4a16_status w4a16_gemm(const void *a, const int32_t *b_q, const void *scales, const int32_t *qzeros,
-                        int group_size, int zp_bias, const void *bias, void *out, int64_t m,
-                        int64_t k, int64_t n, w4a16_dtype dtype, w4a16_stream_t stream) {
-  GemmArgs g{a, b_q, scales, qzeros, group_size, zp_bias, bias, out, m, k, n, static_cast<int>(dtype),
-             reinterpret_cast<cudaStream_t>(stream)};
+static w4a16_status gemm_impl(GemmArgs &g) {
   w4a16_status st = validate_gemm(g);
   if (st != W4A16_OK) return st;
-  if (m == 0) return ok();
+  if (g.M == 0) return ok();
+  if (g.workspace && !aligned(g.workspace, 256))
+    return fail(W4A16_ERR_MISALIGNED, "workspace must be 256-byte aligned");
   DeviceInfo dev;
   cudaError_t e = current_device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "device query");
   w4a16_plan_t plan;
-  choose_plan(g, dev.num_sms, tma_available(), /*query_device=*/true, &plan);
+  bool ws = false;
+  if (g.workspace) {
+    const size_t need = prefill_workspace_bytes(g.M, g.K, g.N, g.group_size, dev.num_sms);
+    ws = need > 0 && g.workspace_bytes >= need;
+  }
+  choose_plan(g, dev.num_sms, tma_available(), /*query_device=*/true, ws, &plan);
   switch (plan.path) {
     case W4A16_PATH_DECODE: e = launch_gemm_decode(g, plan); break;
     case W4A16_PATH_PREFILL: e = launch_gemm_prefill(g, plan); break;
@@ -315,8 +318,42 @@ w4a16_status w4a16_gemm(const void *a, const int32_t *b_q, const void *scales, c
   return ok();
 }
 
+w4a16_status w4a16_gemm(const void *a, const int32_t *b_q, const void *scales, const int32_t *qzeros,
+                        int group_size, int zp_bias, const void *bias, void *out, int64_t m,
+                        int64_t k, int64_t n, w4a16_dtype dtype, w4a16_stream_t stream) {
+  GemmArgs g{a, b_q, scales, qzeros, group_size, zp_bias, bias, out, m, k, n, static_cast<int>(dtype),
+             reinterpret_cast<cudaStream_t>(stream)};
+  return gemm_impl(g);
+}
+
+w4a16_status w4a16_gemm_ws(const void *a, const int32_t *b_q, const void *scales, const int32_t *qzeros,
+                           int group_size, int zp_bias, const void *bias, void *out, int64_t m, int64_t k,
+                           int64_t n, w4a16_dtype dtype, void *workspace, size_t workspace_bytes,
+                           w4a16_stream_t stream) {
+  GemmArgs g{a, b_q, scales, qzeros, group_size, zp_bias, bias, out, m, k, n, static_cast<int>(dtype),
+             reinterpret_cast<cudaStream_t>(stream)};
+  g.workspace = workspace;
+  g.workspace_bytes = workspace ? workspace_bytes : 0;
+  if (workspace) {
+    const Range w = range(workspace, static_cast<int64_t>(workspace_bytes));
+    const int64_t ng = (group_size > 0 && k > 0) ? k / group_size : 0;
+    if (overlaps(w, range(out, m * n * 2)) || overlaps(w, range(a, m * k * 2)) ||
+        overlaps(w, range(b_q, k * n / 2)) || overlaps(w, range(scales, ng * n * 2)) ||
+        (qzeros && overlaps(w, range(qzeros, ng * n / 2))) || (bias && overlaps(w, range(bias, n * 2))))
+      return fail(W4A16_ERR_INVALID_ARG, "workspace overlaps a tensor argument");
+  }
+  return gemm_impl(g);
+}
+
+size_t w4a16_gemm_workspace_size(int64_t m, int64_t k, int64_t n, int group_size, int dtype) {
+  if (check_config(k, n, group_size, dtype) != W4A16_OK || m <= 0) return 0;
+  DeviceInfo dev;
+  if (current_device_info(&dev) != cudaSuccess) return 0;
+  return prefill_workspace_bytes(m, k, n, group_size, dev.num_sms);
+}
+
 w4a16_status w4a16_plan(int64_t m, int64_t k, int64_t n, int group_size, int dtype, int has_zp,
-                        int num_sms, w4a16_plan_t *plan) {
+                        int num_sms, int with_workspace, w4a16_plan_t *plan) {
   if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan must not be NULL");
   w4a16_status st = check_config(k, n, group_size, dtype);
   if (st != W4A16_OK) return st;
@@ -335,13 +372,13 @@ w4a16_status w4a16_plan(int64_t m, int64_t k, int64_t n, int group_size, int dty
   GemmArgs g{p16, static_cast<const int32_t *>(p16), p16, has_zp ? static_cast<const int32_t *>(p16) : nullptr,
              group_size, 8, nullptr, nullptr, m, k, n, dtype, nullptr};
   // a host-only query: assume a GPU driver; use the device's occupancy only when it was asked for
-  choose_plan(g, num_sms, /*tma=*/true, query_device, plan);
+  choose_plan(g, num_sms, /*tma=*/true, query_device, with_workspace != 0, plan);
   return ok();
 }
 
 int w4a16_debug_selected_path(int64_t m, int64_t k, int64_t n, int group_size) {
   w4a16_plan_t p;
-  if (w4a16_plan(m, k, n, group_size, W4A16_F16, 0, 0, &p) != W4A16_OK) return -1;
+  if (w4a16_plan(m, k, n, group_size, W4A16_F16, 0, 0, 0, &p) != W4A16_OK) return -1;
   return p.path;
 }
 

@@ -502,7 +502,7 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
   p->warps = kConsumers + 1;
   p->grid = n_tiles * C;
   p->smem_bytes = J == 1 ? Layout<1>::kSmem : Layout<2>::kSmem;
-  p->reserved = static_cast<int32_t>((kbt + C - 1) / C);
+  p->stream_k = 0;
 }
 
 bool decode_supported(const GemmArgs &g) { return decode_supported_impl(g); }

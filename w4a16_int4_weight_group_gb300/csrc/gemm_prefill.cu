@@ -28,6 +28,7 @@
 //    TMEM and exits without writing output.
 //  * Epilogue: tcgen05.ld 32 columns at a time, + bias in fp32, one rounding to the dtype, 16-byte
 //    stores (PR #40977 report, key source snippets, test reference: bias before the cast).
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -59,7 +60,7 @@ struct PLayout {
   static constexpr int kOffS = kOffP + SA * kPBytes;
   static constexpr int kOffZ = kOffS + SA * kSBytes;
   static constexpr int kOffBar = kOffZ + SA * kZBytes;
-  static constexpr int kNumBars = 2 * SA + 2 * SB + 2;  // + accumulator-full and the stall-test barrier
+  static constexpr int kNumBars = 2 * SA + 2 * SB + 4;  // + accumulator full/empty, epilogue done, stall test
   static constexpr int kOffSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffFlag = kOffSlot + 4;
   static constexpr int kSmemUsed = kOffFlag + 4;
@@ -127,8 +128,24 @@ struct PrefillParams {
   int64_t M, K, N;
   int G;
   int zp_bias;
-  int nk;     // K blocks of 64
+  int nk;            // K blocks of 64
+  int m_tiles;       // row tiles; tile t covers rows (t % m_tiles) and columns (t / m_tiles)
+  int64_t tiles;     // m_tiles x column tiles
+  float *partials;   // stream-K: one fp32 [BM][BN] partial tile per CTA (null when every CTA owns whole tiles)
+  unsigned int *flags;  // stream-K: per-CTA "partial ready" flags; zero before and after every launch
 };
+
+// First (tile, K block) work unit of CTA c when the tiles x nk units are split evenly over G CTAs.
+__device__ __forceinline__ int64_t unit_begin(int64_t c, int64_t total, int64_t G) { return c * total / G; }
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned int *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 template <bool BF>
 __device__ __forceinline__ void magic4(uint32_t w, uint32_t (&h)[4]) {
@@ -167,8 +184,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t m0 = int64_t(blockIdx.x) * BM;
-  const int64_t n0 = int64_t(blockIdx.y) * BN;
+
+  // Work units are (tile, K block) pairs, tile-major; CTA c takes a contiguous, even share. With one
+  // CTA per tile every share is a whole tile; with fewer CTAs (stream-K) a share may start or end
+  // inside a tile: the CTA holding a tile's K block 0 owns it and adds the partial tiles of the
+  // CTAs that hold the rest (they publish them in the workspace) before the epilogue.
+  const int nk = p.nk;
+  const int64_t total = p.tiles * nk;
+  const int64_t G = gridDim.x;
+  const int64_t u_begin = unit_begin(blockIdx.x, total, G);
+  const int64_t u_end = unit_begin(int64_t(blockIdx.x) + 1, total, G);
+  const int n_units = static_cast<int>(u_end - u_begin);
+  const int64_t t_first = u_begin / nk;
+  const int kb_first = static_cast<int>(u_begin - t_first * nk);
 
   const uint32_t bar0 = base + kOffBar;
   auto full_a = [&](int s) { return bar0 + 8u * s; };
@@ -176,7 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto full_b = [&](int s) { return bar0 + 8u * (2 * SA + s); };
   auto empty_b = [&](int s) { return bar0 + 8u * (2 * SA + SB + s); };
   const uint32_t accum_full = bar0 + 8u * (2 * SA + 2 * SB);
-  const uint32_t stall_bar = accum_full + 8u;
+  const uint32_t accum_empty = accum_full + 8u;
+  const uint32_t epi_done = accum_empty + 8u;  // the epilogue warps' stores of a split tile are done
+  const uint32_t stall_bar = epi_done + 8u;
   const uint32_t abort_flag = base + kOffFlag;
   const uint32_t slot = base + kOffSlot;
 
@@ -193,6 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty_b(s), 1);
     }
     mbar_init(accum_full, 1);
+    mbar_init(accum_empty, kDequantWarps);
+    mbar_init(epi_done, kDequantWarps);
     mbar_init(stall_bar, 1);
     st_flag(abort_flag, 0u);
     mbar_init_fence();
@@ -214,7 +246,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch_dependents();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(base_ptr + kOffSlot);
 
-  const int nk = p.nk;
   constexpr int srows = TWO_GROUPS ? 2 : 1;  // G = 32: a K block spans two scale groups
 
   if (warp == 0) {
@@ -222,22 +253,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t tx = kABytes + kPBytes + srows * (BN * 2) + (HAS_ZP ? srows * (BN / 8) * 4 : 0);
       int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % SA;
-        const uint32_t ph = (kb / SA) & 1;
+      int64_t t = t_first;
+      int kb = kb_first;
+      for (int i = 0; i < n_units; ++i) {
+        const int s = i % SA;
+        const uint32_t ph = (i / SA) & 1;
         if (!wait_phase(empty_a(s), ph ^ 1u, abort_flag, limit_ns, &g_prefill_error)) break;
         mbar_arrive_expect_tx(full_a(s), tx);
+        const int m0 = static_cast<int>((t % p.m_tiles) * BM);
+        const int n0 = static_cast<int>((t / p.m_tiles) * BN);
         const int k0 = kb * BK;
         const int grow = k0 / p.G;
-        tma_load_2d(base + kOffA + s * kABytes, &tmA, k0, static_cast<int>(m0), full_a(s));
-        tma_load_2d(base + kOffP + s * kPBytes, &tmP, static_cast<int>(n0 / 8), k0, full_a(s));
-        tma_load_2d(base + kOffS + s * kSBytes, &tmS, static_cast<int>(n0), grow, full_a(s));
-        if constexpr (HAS_ZP) tma_load_2d(base + kOffZ + s * kZBytes, &tmZ, static_cast<int>(n0 / 8), grow, full_a(s));
-        issued = kb + 1;
+        tma_load_2d(base + kOffA + s * kABytes, &tmA, k0, m0, full_a(s));
+        tma_load_2d(base + kOffP + s * kPBytes, &tmP, n0 / 8, k0, full_a(s));
+        tma_load_2d(base + kOffS + s * kSBytes, &tmS, n0, grow, full_a(s));
+        if constexpr (HAS_ZP) tma_load_2d(base + kOffZ + s * kZBytes, &tmZ, n0 / 8, grow, full_a(s));
+        issued = i + 1;
+        if (++kb == nk) {
+          kb = 0;
+          ++t;
+        }
       }
       if (ld_flag(abort_flag)) {
         // let this CTA's own copies land before its shared memory is released
-        for (int kb = issued - 1; kb >= 0 && kb >= issued - SA; --kb) drain_phase(full_a(kb % SA), (kb / SA) & 1, &g_prefill_error);
+        for (int i = issued - 1; i >= 0 && i >= issued - SA; --i) drain_phase(full_a(i % SA), (i / SA) & 1, &g_prefill_error);
       }
     }
   } else if (warp == 1) {
@@ -251,10 +290,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                              | (uint32_t(BN >> 3) << 17)       // N
                              | (uint32_t(128 >> 4) << 24);     // M (one MMA per 128-row half)
       bool ok = true;
-      for (int kb = 0; kb < nk && ok; ++kb) {
-        const int sa = kb % SA, sb = kb % SB;
-        ok = wait_phase(full_a(sa), (kb / SA) & 1, abort_flag, limit_ns, &g_prefill_error) &&
-             wait_phase(full_b(sb), (kb / SB) & 1, abort_flag, limit_ns, &g_prefill_error);
+      int kb = kb_first, seg = 0;
+      bool seg_start = true;
+      for (int i = 0; i < n_units && ok; ++i) {
+        const int sa = i % SA, sb = i % SB;
+        if (seg_start && seg > 0) {
+          // the epilogue of the previous segment has read the accumulators out of TMEM
+          ok = wait_phase(accum_empty, (seg - 1) & 1, abort_flag, limit_ns, &g_prefill_error);
+          if (!ok) break;
+        }
+        ok = wait_phase(full_a(sa), (i / SA) & 1, abort_flag, limit_ns, &g_prefill_error) &&
+             wait_phase(full_b(sb), (i / SB) & 1, abort_flag, limit_ns, &g_prefill_error);
         if (!ok) break;
         tc_fence_after();
         const uint32_t a_base = base + kOffA + sa * kABytes;
@@ -269,19 +315,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; a K step of 16 is 32 bytes;
             // rows 128*mt.. start 16 KB further. Accumulator mt lives in TMEM columns 256*mt..
             const uint64_t ad = smem_desc(a_base + 16384u * mt + 32u * kk, 16u, 1024u);
-            umma_f16(tmem + 256u * mt, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_f16(tmem + 256u * mt, ad, bd, idesc, (seg_start && kk == 0) ? 0u : 1u);
           }
         }
         umma_commit(empty_a(sa));
         umma_commit(empty_b(sb));
+        seg_start = false;
+        const bool seg_end = (kb == nk - 1) || (i == n_units - 1);
+        if (seg_end) {
+          umma_commit(accum_full);  // segment `seg` accumulated: hand it to the epilogue
+          ++seg;
+          seg_start = true;
+        }
+        if (++kb == nk) kb = 0;
       }
-      umma_commit(accum_full);
-      if (!ok) drain_phase(accum_full, 0, &g_prefill_error);
+      if (!ok) {
+        umma_commit(accum_full);
+        drain_phase(accum_full, seg & 1, &g_prefill_error);
+      }
     }
   } else {
-    // ------------------------------------------------------------ dequantisers
+    // ------------------------------------------------------------ dequantisers, then epilogues
     const int dw = warp - 2;  // 0..7
     const int c = lane;       // packed word column of the tile (8 output columns)
+    const int q = warp & 3;   // TMEM lane quarter this warp may read
+    const int row = 32 * q + lane;
+    const int half = dw >> 2;  // epilogue columns [128*half, 128*half + 128)
     bool ok = true;
     uint32_t zsub[2][4], spair[2][4];
     if constexpr (!HAS_ZP) {
@@ -299,10 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = wait_phase(stall_bar, 0, abort_flag, limit_ns, &g_prefill_error);
       ok = __all_sync(0xffffffffu, ok);
     }
-    for (int kb = 0; kb < nk && ok; ++kb) {
-      const int sa = kb % SA, sb = kb % SB;
-      ok = wait_phase(full_a(sa), (kb / SA) & 1, abort_flag, limit_ns, &g_prefill_error) &&
-           wait_phase(empty_b(sb), ((kb / SB) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error);
+    int64_t t = t_first;
+    int kb = kb_first, seg = 0, seg_kb0 = kb_first, epi_uses = 0;
+    for (int i = 0; i < n_units && ok; ++i) {
+      const int sa = i % SA, sb = i % SB;
+      ok = wait_phase(full_a(sa), (i / SA) & 1, abort_flag, limit_ns, &g_prefill_error) &&
+           wait_phase(empty_b(sb), ((i / SB) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error);
       ok = __all_sync(0xffffffffu, ok);  // the warp leaves the loop together
       if (!ok) break;
       const uint32_t P = base + kOffP + sa * kPBytes;
@@ -322,9 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 #pragma unroll
-      for (int i = 0; i < BK / kDequantWarps; ++i) {
-        const int r = dw + kDequantWarps * i;
-        const int gr = (TWO_GROUPS && i >= BK / kDequantWarps / 2) ? 1 : 0;  // rows 32..63: second group
+      for (int ii = 0; ii < BK / kDequantWarps; ++ii) {
+        const int r = dw + kDequantWarps * ii;
+        const int gr = (TWO_GROUPS && ii >= BK / kDequantWarps / 2) ? 1 : 0;  // rows 32..63: second group
         const uint32_t wq = lds32(P + r * (BN / 2) + c * 4);
         uint32_t h[4];
         magic4<BF>(wq, h);
@@ -344,31 +405,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(full_b(sb));
         mbar_arrive(empty_a(sa));
       }
-    }
 
-    // ------------------------------------------------------------ epilogue
-    if (ok) ok = wait_phase(accum_full, 0, abort_flag, limit_ns, &g_prefill_error);
-    ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
-    tc_fence_after();
-    const int q = warp & 3;                // TMEM lane quarter this warp may read
-    const int row = 32 * q + lane;
-    const int half = dw >> 2;              // columns [128*half, 128*half + 128)
+      const bool seg_end = (kb == nk - 1) || (i == n_units - 1);
+      if (seg_end) {
+        // ---------------------------------------------------------- epilogue of this segment
+        ok = wait_phase(accum_full, seg & 1, abort_flag, limit_ns, &g_prefill_error);
+        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
+        tc_fence_after();
+        const bool owner = seg_kb0 == 0;        // holds K block 0: adds the others' partials, stores
+        const bool whole = owner && kb == nk - 1;
+        const int64_t m0 = (t % p.m_tiles) * BM;
+        const int64_t n0 = (t / p.m_tiles) * BN;
+        // CTAs whose share starts inside this tile after this one: they hold the rest of it
+        int64_t c_last = blockIdx.x;
+        if (owner && !whole) {
+          while (c_last + 1 < G && unit_begin(c_last + 1, total, G) < (t + 1) * nk) ++c_last;
+          // wait until each of them has published its partial tile (one poller per warp)
+          for (int64_t cc = blockIdx.x + 1; cc <= c_last && ok; ++cc) {
+            if (lane == 0) {
+              const uint64_t t0 = globaltimer();
+              while (ld_acquire_u32(p.flags + cc) == 0u) {
+                if (ld_flag(abort_flag)) { ok = false; break; }
+                if (globaltimer() - t0 > limit_ns) {
+                  st_flag(abort_flag, 1u);
+                  atomicOr(&g_prefill_error, 1u);
+                  ok = false;
+                  break;
+                }
+              }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();  // orders lane 0's acquire before every lane's reads of the partial tile
+          }
+        }
 #pragma unroll 1
-    for (int it = 0; it < 4 * MT; ++it) {
-      const int mt = it >> 2, ch = it & 3;  // accumulator (row half of the tile) and 32-column chunk
-      const int64_t m = m0 + 128 * mt + row;
-      const bool row_ok = m < p.M;
-      const int col0 = half * 128 + ch * 32;
-      uint32_t r[32];
-      if (ok) {
-        tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(256 * mt + col0), r);
-        tmem_wait_ld();
-      }
-      if (ok && row_ok) {
+        for (int it = 0; it < 4 * MT; ++it) {
+          const int mt = it >> 2, ch = it & 3;  // accumulator (row half of the tile) and 32-column chunk
+          const int tr = 128 * mt + row;        // row within the tile
+          const int64_t m = m0 + tr;
+          const bool row_ok = m < p.M;
+          const int col0 = half * 128 + ch * 32;
+          uint32_t r[32];
+          if (ok) {
+            tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(256 * mt + col0), r);
+            tmem_wait_ld();
+          }
+          if (!ok) continue;
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {
-          const int64_t n = n0 + col0 + 8 * g8;
-          if (n < p.N) {
+          for (int g8 = 0; g8 < 4; ++g8) {
             // accumulator columns hold outputs n+0, n+4, n+1, n+5, n+2, n+6, n+3, n+7
             float v[8];
             v[0] = __uint_as_float(r[8 * g8 + 0]);
@@ -379,6 +463,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[6] = __uint_as_float(r[8 * g8 + 5]);
             v[3] = __uint_as_float(r[8 * g8 + 6]);
             v[7] = __uint_as_float(r[8 * g8 + 7]);
+            const int tc = col0 + 8 * g8;  // column within the tile
+            if (!owner) {
+              // publish this CTA's partial tile (row-major fp32 [BM][BN])
+              float4 *dst = reinterpret_cast<float4 *>(p.partials + (int64_t(blockIdx.x) * BM + tr) * BN + tc);
+              dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+              dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+              continue;
+            }
+            // owner: add the partials of the following CTAs in order (deterministic), then store
+            for (int64_t cc = int64_t(blockIdx.x) + 1; cc <= c_last; ++cc) {
+              const float4 *src = reinterpret_cast<const float4 *>(p.partials + (cc * BM + tr) * BN + tc);
+              const float4 a0 = __ldcg(src), a1 = __ldcg(src + 1);  // L2: written by another SM
+              v[0] += a0.x; v[1] += a0.y; v[2] += a0.z; v[3] += a0.w;
+              v[4] += a1.x; v[5] += a1.y; v[6] += a1.z; v[7] += a1.w;
+            }
+            const int64_t n = n0 + tc;
+            if (!row_ok || n >= p.N) continue;
             if (p.bias) {
               const uint4 bv = *reinterpret_cast<const uint4 *>(p.bias + n);
               const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
@@ -392,16 +493,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               if constexpr (BF) {
-                const __nv_bfloat162 t = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-                o[e] = *reinterpret_cast<const uint32_t *>(&t);
+                const __nv_bfloat162 tt = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                o[e] = *reinterpret_cast<const uint32_t *>(&tt);
               } else {
-                const __half2 t = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
-                o[e] = *reinterpret_cast<const uint32_t *>(&t);
+                const __half2 tt = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
+                o[e] = *reinterpret_cast<const uint32_t *>(&tt);
               }
             }
             *reinterpret_cast<uint4 *>(p.out + m * p.N + n) = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
+        // the accumulators have been read: the next segment's MMAs may overwrite them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(accum_empty);
+        // partial tiles: publish (contributor) or release the consumed flags (owner), once every
+        // epilogue warp is done with its stores / reads (a bounded mbarrier wait, not a hard barrier)
+        if (!whole) {
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(epi_done);
+          if (dw == 0 && lane == 0) {
+            if (wait_phase(epi_done, epi_uses & 1, abort_flag, limit_ns, &g_prefill_error)) {
+              if (!owner) {
+                st_release_u32(p.flags + blockIdx.x, 1u);
+              } else {
+                for (int64_t cc = int64_t(blockIdx.x) + 1; cc <= c_last; ++cc) p.flags[cc] = 0u;
+              }
+            }
+          }
+          ++epi_uses;
+        }
+        if (!ok) break;
+        ++seg;
+        seg_kb0 = 0;
+      }
+      if (++kb == nk) {
+        kb = 0;
+        ++t;
       }
     }
   }
@@ -436,17 +565,27 @@ int smem_of(int MT) { return MT == 2 ? PLayout<2>::kSmemBytes : PLayout<1>::kSme
 }  // namespace
 
 bool prefill_supported(const GemmArgs &g) {
+  const int64_t tiles = ((g.M + 127) / 128) * ((g.N + BN - 1) / BN);
   return g.N % 32 == 0 && g.K % 8 == 0 && aligned16(g.a) && aligned16(g.b_q) && aligned16(g.scales) &&
          aligned16(g.out) && (g.qzeros == nullptr || aligned16(g.qzeros)) && (g.bias == nullptr || aligned16(g.bias)) &&
-         (g.N + BN - 1) / BN <= 65535;
+         tiles <= 0x7fffffff;
 }
 
-void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, w4a16_plan_t *p) {
-  (void)K;
+size_t prefill_workspace_bytes(int64_t M, int64_t K, int64_t N, int group_size, int num_sms) {
+  w4a16_plan_t pl;
+  prefill_make_plan(M, K, N, group_size, num_sms, /*workspace=*/true, &pl);
+  if (!pl.stream_k) return 0;
+  // one fp32 partial tile and one flag per CTA
+  return static_cast<size_t>(pl.grid) * pl.m_tile * BN * sizeof(float) + static_cast<size_t>(pl.grid) * 4 + 256;
+}
+
+void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool workspace,
+                       w4a16_plan_t *p) {
   (void)group_size;
   // One CTA per SM (shared memory). Two 128-row accumulators halve the dequantisation work per
   // FLOP, which makes a tile-row about 1.4x cheaper (measured); pick the smaller waves x work.
   const int64_t n_tiles = (N + BN - 1) / BN;
+  const int64_t nk = (K + BK - 1) / BK;
   double best_cost = -1.0;
   int MT = 1;
   for (int mt = 2; mt >= 1; --mt) {
@@ -457,15 +596,25 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
       MT = mt;
     }
   }
+  int64_t tiles = ((M + 128 * MT - 1) / (128 * MT)) * n_tiles;
+  const int64_t waves = (tiles + num_sms - 1) / num_sms;
+  const double fill = double(tiles) / double(waves * num_sms);
+  // Stream-K when whole tiles leave SMs idle in the last wave and a workspace is available: every SM
+  // gets the same number of (tile, K block) units. Two accumulators then always pay off.
+  const bool stream_k = workspace && fill < 0.85 && M > 128;
+  if (stream_k) {
+    MT = 2;
+    tiles = ((M + 255) / 256) * n_tiles;
+  }
   p->path = W4A16_PATH_PREFILL;
   p->words_per_lane = 1;
   p->m_tile = 128 * MT;
   p->n_tile = BN;
   p->k_split = 1;
   p->warps = kThreads / 32;
-  p->grid = ((M + 128 * MT - 1) / (128 * MT)) * n_tiles;
+  p->grid = stream_k ? std::min<int64_t>(num_sms, tiles * nk) : tiles;
   p->smem_bytes = smem_of(MT);
-  p->reserved = 0;
+  p->stream_k = stream_k ? 1 : 0;
 }
 
 cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl) {
@@ -501,6 +650,17 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl) {
     }
   }
   PrefillParams prm;
+  prm.m_tiles = static_cast<int>((g.M + BM - 1) / BM);
+  prm.tiles = int64_t(prm.m_tiles) * ((g.N + BN - 1) / BN);
+  prm.partials = nullptr;
+  prm.flags = nullptr;
+  if (pl.stream_k) {
+    // workspace: [grid][BM][BN] fp32 partial tiles, then [grid] flags (zero between calls)
+    const size_t part_bytes = static_cast<size_t>(pl.grid) * BM * BN * sizeof(float);
+    if (!g.workspace || g.workspace_bytes < part_bytes + static_cast<size_t>(pl.grid) * 4) return cudaErrorInvalidValue;
+    prm.partials = static_cast<float *>(g.workspace);
+    prm.flags = reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(g.workspace) + part_bytes);
+  }
   prm.bias = static_cast<const uint16_t *>(g.bias);
   prm.out = static_cast<uint16_t *>(g.out);
   prm.M = g.M;
@@ -511,7 +671,7 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl) {
   prm.nk = static_cast<int>((g.K + BK - 1) / BK);
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((g.M + BM - 1) / BM), static_cast<unsigned>((g.N + BN - 1) / BN), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_of(MT);
   cfg.stream = g.stream;

@@ -21,6 +21,8 @@ struct GemmArgs {
   int64_t M, K, N;
   int dtype;  // w4a16_dtype
   cudaStream_t stream;
+  void *workspace = nullptr;     // optional caller-owned scratch (w4a16_gemm_ws)
+  size_t workspace_bytes = 0;
 };
 
 struct DeviceInfo {
@@ -63,7 +65,10 @@ cudaError_t decode_set_stall(bool on);
 
 // Prefill path (tcgen05).
 bool prefill_supported(const GemmArgs &g);
-void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, w4a16_plan_t *p);
+// workspace: a scratch buffer will be available (stream-K may be chosen).
+void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool workspace,
+                       w4a16_plan_t *p);
+size_t prefill_workspace_bytes(int64_t M, int64_t K, int64_t N, int group_size, int num_sms);
 cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &p);
 // Reads and clears the device error word of the prefill kernels on the current device.
 cudaError_t prefill_take_device_error(uint32_t *err);
