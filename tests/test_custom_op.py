@@ -58,6 +58,7 @@ def test_compiled_op_uses_runtime_m(ops):
                        dynamic=True)
     for M in (1024, 1, 8, 512):
         c = synth.make_case(M, K, N, G, "f16", asym=True, bias=True, seed=31)
+        c.bias = base.bias  # the weights match the base case (drawn first); the bias is drawn after A
         out = fn(bits_to_torch(c.a, "f16"))
         torch.cuda.synchronize()
         rows = np.unique(np.linspace(0, M - 1, 6).astype(int))
