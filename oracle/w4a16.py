@@ -116,9 +116,10 @@ def dequant_t(b_q, scales, qzeros, group_size: int, zp_bias: int, dtype: str, co
 def gemm_ref(a, b_q, scales, qzeros, group_size: int, zp_bias: int, bias, dtype: str, *,
              weights: str = "dequant_t", rows=None, cols=None) -> np.ndarray:
     """fp64 [M, N] = A . W (+ bias), no final cast. ``rows``/``cols`` select a sub-block."""
-    A = t_decode(np.asarray(a), dtype)
+    a = np.asarray(a)
     if rows is not None:
-        A = A[np.asarray(rows, dtype=np.int64)]
+        a = a[np.asarray(rows, dtype=np.int64)]
+    A = t_decode(a, dtype)
     N = b_q.shape[1] * 8
     cols = np.arange(N) if cols is None else np.asarray(cols, dtype=np.int64)
     W = dequant_exact(b_q, scales, qzeros, group_size, zp_bias, dtype, cols)
@@ -138,9 +139,10 @@ def weight_rounding_bound(a, b_q, scales, qzeros, group_size, zp_bias, dtype, *,
 
     A rigorous bound on |gemm_ref(dequant_t) - gemm_ref(exact)| (up to fp64 rounding).
     """
-    A = np.abs(t_decode(np.asarray(a), dtype))
+    a = np.asarray(a)
     if rows is not None:
-        A = A[np.asarray(rows, dtype=np.int64)]
+        a = a[np.asarray(rows, dtype=np.int64)]
+    A = np.abs(t_decode(a, dtype))
     W = dequant_exact(b_q, scales, qzeros, group_size, zp_bias, dtype, cols)
     Wt = t_decode(t_encode_rne(W, dtype), dtype)
     return A @ np.abs(Wt - W)

@@ -50,8 +50,9 @@ def forced_path(path):
 
 
 def sample_cols(N: int, rng: np.random.Generator, k: int = 384) -> np.ndarray:
-    """Columns to check on wide outputs: both edges, every n % 8 position, tile edges, random."""
-    base = set(range(0, min(N, 272))) | set(range(max(0, N - 272), N))
+    """Columns to check on wide outputs: both edges (past the first and into the last 256-column
+    tile, every n % 8 position), and k random ones."""
+    base = set(range(0, min(N, 264))) | set(range(max(0, N - 264), N))
     base |= set(rng.integers(0, N, size=k).tolist())
     return np.array(sorted(base), dtype=np.int64)
 
