@@ -7,14 +7,15 @@
 // the GPU idle. What this kernel does on sm_103a:
 //
 //  * Work split. A CTA owns 256 output columns and a contiguous range of K blocks (64 rows each);
-//    the C CTAs of one thread-block cluster split K. Nine warps: one TMA producer and eight
-//    consumers, consumer w owning columns [32w, 32w+32) of the tile for the whole K range, so no
-//    reduction is needed inside the CTA. Cluster ranks add their partial tiles through distributed
-//    shared memory in a fixed order: deterministic, and no global scratch memory.
+//    the C CTAs of one thread-block cluster split K. Seventeen warps: one TMA producer and sixteen
+//    consumers in two groups of eight that take alternate K blocks; consumer w of a group owns
+//    columns [32w, 32w+32) of the tile. The second group hands its sums to the first through
+//    shared memory, and cluster ranks add their partial tiles through distributed shared memory,
+//    both in a fixed order: deterministic, and no global scratch memory.
 //  * Streaming. Per K block one TMA box of packed weights (64 rows x 128 bytes, 128-byte swizzle),
 //    the activation rows (8 or 16 x 64, zero-filled past M), and the scale and zero-point rows of the
-//    block's one or two groups land in an 8-deep ring of shared-memory stages guarded by full/empty
-//    mbarriers; the producer runs up to 8 blocks ahead, so 64 KB per CTA are in flight.
+//    block's one or two groups land in a 16-deep ring of shared-memory stages guarded by full/empty
+//    mbarriers; the producer runs up to 16 blocks ahead, so 128 KB of weights per CTA are in flight.
 //  * Fragments. Viewing a packed row as 16-bit elements (4 nibbles = 4 consecutive columns each),
 //    ldmatrix.trans delivers to lane (g, t) the element of rows 2t and 2t+1 for column quad g: the
 //    two rows of a k pair side by side, which is what a 16-bit MMA register holds. The 128-byte
@@ -309,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------------------------ reduction and epilogue
+  __syncwarp();  // the producer warp's lanes meet again before the warp-aligned barriers below
   // group 1 hands its partial sums to group 0 (fixed order: group 0 + group 1)
   {
     float *gred = reinterpret_cast<float *>(base_ptr + L::kOffGRed);
@@ -325,7 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           gred[(m + 1) * BN + nl + q + 2] = acc[jt][q][3];
         }
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");  // consumer warps only
+    // named barrier of the 16 consumer warps: the producer warp must not arrive on it (a 17th warp
+    // would open a second phase of the barrier that nobody completes)
+    if (warp < kConsumers) asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
     if (warp < kBlocksPerRow) {
 #pragma unroll
       for (int jt = 0; jt < J; ++jt)
