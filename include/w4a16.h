@@ -157,6 +157,29 @@ w4a16_status w4a16_gemm_ws(const void *a, const int32_t *b_q, const void *scales
                            int64_t n, w4a16_dtype dtype, void *workspace, size_t workspace_bytes,
                            w4a16_stream_t stream);
 
+/*
+ * w4a16_gemm_noalloc - w4a16_gemm_ws without a caller-provided workspace and without allocating:
+ * for callers that cannot call cudaMalloc - e.g. code running while a CUDA graph is being captured
+ * (allocation is not capturable), allocator-less runtimes and plugins handed only tensor pointers, or
+ * hosts that forbid device allocations after start-up. The paper has no counterpart; it is an
+ * addition of this library.
+ *   The scratch is a static device array inside the library (40 MiB + 4 KiB: stream-K partial tiles
+ *   for up to 160 CTAs and their flags). Every GPU that loads the library holds it until the process
+ *   exits. The first call on a device looks its address up (cudaGetSymbolAddress) with that device
+ *   current; make that first call before any stream capture.
+ *   Every call on a device shares the one array, which keeps the previous call's contents: the call
+ *   clears the part that must start at zero (the flags) on `stream` first. Calls that overlap on the
+ *   GPU (other streams, other threads, graphs replayed concurrently) race on it: serialise them.
+ *   A call whose plan needs more scratch than the array holds (stream-K on a device with more than
+ *   160 SMs) is rejected with W4A16_ERR_UNSUPPORTED and the sizes in the message.
+ * It calls no cudaMalloc, cudaFree or allocating library routine. Arguments, results and other
+ * errors are those of w4a16_gemm.
+ */
+w4a16_status w4a16_gemm_noalloc(const void *a, const int32_t *b_q, const void *scales,
+                                const int32_t *qzeros, int group_size, int zp_bias, const void *bias,
+                                void *out, int64_t m, int64_t k, int64_t n, w4a16_dtype dtype,
+                                w4a16_stream_t stream);
+
 /* Bytes of workspace w4a16_gemm_ws can use for these sizes on the current device (0: none). */
 size_t w4a16_gemm_workspace_size(int64_t m, int64_t k, int64_t n, int group_size, int dtype);
 

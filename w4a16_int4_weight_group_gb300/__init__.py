@@ -54,6 +54,8 @@ SIGNATURES = [
     ("w4a16_gemm_ws", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_int, _vp,
                                ctypes.c_size_t, _vp]),
     ("w4a16_gemm_workspace_size", ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_int, _c_int]),
+    ("w4a16_gemm_noalloc", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_int,
+                                    _vp]),
     ("w4a16_can_implement", _c_int, [_c_i64, _c_i64, _c_int, _c_int, _c_int]),
     ("w4a16_plan", _c_int, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(Plan)]),
     ("w4a16_last_error", ctypes.c_char_p, []),

@@ -345,6 +345,43 @@ w4a16_status w4a16_gemm_ws(const void *a, const int32_t *b_q, const void *scales
   return gemm_impl(g);
 }
 
+w4a16_status w4a16_gemm_noalloc(const void *a, const int32_t *b_q, const void *scales,
+                                const int32_t *qzeros, int group_size, int zp_bias, const void *bias,
+                                void *out, int64_t m, int64_t k, int64_t n, w4a16_dtype dtype,
+                                w4a16_stream_t stream) {
+  GemmArgs g{a, b_q, scales, qzeros, group_size, zp_bias, bias, out, m, k, n, static_cast<int>(dtype),
+             reinterpret_cast<cudaStream_t>(stream)};
+  w4a16_status st = validate_gemm(g);
+  if (st != W4A16_OK) return st;
+  if (m == 0) return ok();
+  DeviceInfo dev;
+  cudaError_t e = current_device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  void *scratch = nullptr;
+  size_t scratch_bytes = 0;
+  e = prefill_static_scratch(&scratch, &scratch_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "static scratch address (cudaGetSymbolAddress)");
+  const size_t need = prefill_workspace_bytes(m, k, n, group_size, dev.num_sms);
+  if (need > scratch_bytes)
+    return fail(W4A16_ERR_UNSUPPORTED,
+                "this call needs %zu bytes of scratch (stream-K over %d SMs); the static scratch holds %zu",
+                need, dev.num_sms, scratch_bytes);
+  if (need > 0) {
+    // The array keeps the previous call's contents: the stream-K flags must start at zero.
+    w4a16_plan_t plan;
+    choose_plan(g, dev.num_sms, tma_available(), /*query_device=*/true, /*workspace=*/true, &plan);
+    if (plan.path == W4A16_PATH_PREFILL && plan.stream_k) {
+      const size_t flags_at = static_cast<size_t>(plan.grid) * plan.m_tile * plan.n_tile * sizeof(float);
+      e = cudaMemsetAsync(static_cast<uint8_t *>(scratch) + flags_at, 0, static_cast<size_t>(plan.grid) * 4,
+                          g.stream);
+      if (e != cudaSuccess) return cuda_fail(e, "clear static scratch flags");
+    }
+  }
+  g.workspace = scratch;
+  g.workspace_bytes = scratch_bytes;
+  return gemm_impl(g);
+}
+
 size_t w4a16_gemm_workspace_size(int64_t m, int64_t k, int64_t n, int group_size, int dtype) {
   if (check_config(k, n, group_size, dtype) != W4A16_OK || m <= 0) return 0;
   DeviceInfo dev;

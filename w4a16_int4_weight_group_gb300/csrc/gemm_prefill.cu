@@ -686,6 +686,37 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl) {
   return cudaSuccess;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Static scratch for callers that cannot allocate device memory (w4a16_gemm_noalloc): room for the
+// stream-K partial tiles of up to kStaticTiles CTAs (two 128x256 fp32 accumulators each) and their
+// flags. It lives in the library's device image, so every GPU that loads the library holds it until
+// the process exits, and every call shares it.
+// ---------------------------------------------------------------------------------------------
+constexpr size_t kStaticTiles = 160;
+constexpr size_t kStaticScratchBytes = kStaticTiles * 256 * BN * sizeof(float) + 4096;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+cudaError_t prefill_static_scratch(void **ptr, size_t *bytes) {
+  static std::mutex mu;
+  static void *addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    // once per device, with that device current: the host-side name of the array is only a
+    // stand-in; the device address comes from the runtime
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  *bytes = kStaticScratchBytes;
+  return cudaSuccess;
+}
+
 cudaError_t prefill_take_device_error(uint32_t *err) {
   uint32_t v = 0, zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_prefill_error, sizeof(v));

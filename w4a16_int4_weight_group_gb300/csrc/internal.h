@@ -69,6 +69,9 @@ bool prefill_supported(const GemmArgs &g);
 void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool workspace,
                        w4a16_plan_t *p);
 size_t prefill_workspace_bytes(int64_t M, int64_t K, int64_t N, int group_size, int num_sms);
+// Device address and size of the library's static scratch array on the current device (looked up
+// once per device).
+cudaError_t prefill_static_scratch(void **ptr, size_t *bytes);
 cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &p);
 // Reads and clears the device error word of the prefill kernels on the current device.
 cudaError_t prefill_take_device_error(uint32_t *err);
