@@ -77,7 +77,7 @@ typedef enum {
 /* Launch plan for one w4a16_gemm call. Filled by w4a16_plan; informational. */
 typedef struct {
   int32_t path;          /* w4a16_path                                                     */
-  int32_t words_per_lane;/* informational (1)                                               */
+  int32_t k_blocks_per_stage; /* decode: 64-row K blocks per pipeline stage (1, 2 or 4); else 1 */
   int32_t m_tile;        /* rows of A per CTA                                              */
   int32_t n_tile;        /* output columns per CTA                                         */
   int32_t k_split;       /* CTAs (one cluster) sharing one output tile along K               */

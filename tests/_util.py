@@ -58,8 +58,10 @@ def sample_cols(N: int, rng: np.random.Generator, k: int = 384) -> np.ndarray:
 
 
 def check_against_oracle(c, out_bits: np.ndarray, rows=None, cols=None, label=""):
-    """Assert |out - ref| <= atol + rtol*|ref| against the dequant-T product, and the rigorous
-    bound against the exact-weight product. Returns a dict of error statistics."""
+    """Accept each output if |out - ref| <= atol + rtol*|ref| for ref = the exact-weight product or
+    ref = the product over the T-rounded dequantised weights (both correct readings of the layer);
+    always require the exact-weight product within tolerance plus the rigorous weight-rounding bound.
+    Returns a dict of error statistics (against the nearer reference)."""
     kw = dict(rows=rows, cols=cols)
     sub = out_bits
     if rows is not None:
@@ -68,20 +70,22 @@ def check_against_oracle(c, out_bits: np.ndarray, rows=None, cols=None, label=""
         sub = sub[:, np.asarray(cols)]
     ref_t = oracle.gemm_ref(c.a, c.b_q, c.scales, c.qzeros, c.G, c.zp_bias, c.bias, c.dtype,
                             weights="dequant_t", **kw)
-    ok = oracle.within_tolerance(sub, ref_t, c.dtype)
-    out = ieee.t_decode(sub, c.dtype)
-    err = np.abs(out - ref_t)
-    atol, rtol = oracle.tolerance(c.dtype)
-    if not ok.all():
-        bad = np.argwhere(~ok)[:8]
-        details = [(int(i), int(j), float(out[i, j]), float(ref_t[i, j])) for i, j in bad]
-        raise AssertionError(f"{label}: {int((~ok).sum())} of {ok.size} outputs outside "
-                             f"{atol}+{rtol}|ref| (max err {err.max():.3g}); first: {details}")
     ref_e = oracle.gemm_ref(c.a, c.b_q, c.scales, c.qzeros, c.G, c.zp_bias, c.bias, c.dtype,
                             weights="exact", **kw)
+    ok = oracle.within_tolerance(sub, ref_t, c.dtype) | oracle.within_tolerance(sub, ref_e, c.dtype)
+    out = ieee.t_decode(sub, c.dtype)
+    atol, rtol = oracle.tolerance(c.dtype)
+    err_t, err_e = np.abs(out - ref_t), np.abs(out - ref_e)
+    use = np.minimum(err_t / (atol + rtol * np.abs(ref_t)), err_e / (atol + rtol * np.abs(ref_e)))
+    if not ok.all():
+        bad = np.argwhere(~ok)[:8]
+        details = [(int(i), int(j), float(out[i, j]), float(ref_t[i, j]), float(ref_e[i, j])) for i, j in bad]
+        raise AssertionError(f"{label}: {int((~ok).sum())} of {ok.size} outputs outside {atol}+{rtol}|ref| of both "
+                             f"references (max err {np.minimum(err_t, err_e).max():.3g}); first (i, j, out, ref_T, ref_E): "
+                             f"{details}")
     bound = oracle.weight_rounding_bound(c.a, c.b_q, c.scales, c.qzeros, c.G, c.zp_bias, c.dtype, **kw)
-    ok_e = np.abs(out - ref_e) <= atol + rtol * np.abs(ref_t) + bound * (1 + 1e-9)
+    ok_e = err_e <= atol + rtol * np.maximum(np.abs(ref_t), np.abs(ref_e)) + bound * (1 + 1e-9)
     if not ok_e.all():
         raise AssertionError(f"{label}: exact-weight bound violated at {int((~ok_e).sum())} outputs")
-    return {"max_err": float(err.max()) if err.size else 0.0,
-            "max_rel_tol_use": float((err / (atol + rtol * np.abs(ref_t))).max()) if err.size else 0.0}
+    return {"max_err": float(np.minimum(err_t, err_e).max()) if use.size else 0.0,
+            "max_rel_tol_use": float(use.max()) if use.size else 0.0}

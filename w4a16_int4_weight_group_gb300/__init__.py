@@ -32,7 +32,7 @@ class W4A16Error(RuntimeError):
 
 
 class Plan(ctypes.Structure):
-    _fields_ = [("path", ctypes.c_int32), ("words_per_lane", ctypes.c_int32), ("m_tile", ctypes.c_int32),
+    _fields_ = [("path", ctypes.c_int32), ("k_blocks_per_stage", ctypes.c_int32), ("m_tile", ctypes.c_int32),
                 ("n_tile", ctypes.c_int32), ("k_split", ctypes.c_int32), ("warps", ctypes.c_int32),
                 ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int32), ("stream_k", ctypes.c_int32)]
 

@@ -20,13 +20,17 @@
 //    ldmatrix.trans delivers to lane (g, t) the element of rows 2t and 2t+1 for column quad g: the
 //    two rows of a k pair side by side, which is what a 16-bit MMA register holds. The 128-byte
 //    swizzle makes the eight row addresses of each 8x8 matrix hit distinct banks.
-//  * Dequantisation (magic numbers, one rounding). One LOP3 places the nibble of column j of both
-//    rows into the low mantissa bits of a packed fp16 pair with exponent of 1024 (64 for the high
-//    nibble of a byte) or a bf16 pair with exponent of 128: the pair is exactly (base+q_k, base+q_k+1).
-//    Subtracting (base+zp) is exact; one packed multiply by the scale rounds once, giving exactly
-//    RNE((q - zp) * s), the values w4a16_dequant writes.
+//  * Dequantisation folded into the product. One LOP3 places the nibble of column j of both rows
+//    of a k pair into the low mantissa bits of a packed fp16 pair with exponent of 1024 (64 for the
+//    high nibble of a byte) or a bf16 pair with exponent of 128: exactly (base+q_k, base+q_k+1).
+//    The tensor core multiplies these exact integers by the activations (blk), and the same
+//    activation fragments by ones (sa = row sums of A over the group's k steps). Per K block and
+//    group, in fp32: acc += s * (blk - (base + zp) * sa), which equals s * sum_k A (q - zp) up to fp32
+//    rounding. The scale is applied in fp32, so the weights are never rounded to 16 bits; with
+//    one-hot activations the result is exactly RNE(s * (q - zp)), the value w4a16_dequant writes.
 //  * Multiply. mma.sync m16n8k16 with 16 output columns as the MMA rows and up to 8 rows of A as the
-//    MMA columns (the M <= 8 decode batch fills the n=8 side; M <= 16 takes two MMAs).
+//    MMA columns (the M <= 8 decode batch fills the n=8 side; M <= 16 takes two MMAs). Per warp and
+//    K block: 8 LOP3-based unpacks of 8 weights each, 12 MMAs (8 products, 4 row sums) and 16 FFMAs.
 //  * Epilogue. Bias is added in fp32 and the sum rounded once to the activation dtype (PR #40977
 //    report, key source snippets, test reference).
 //  * Every mbarrier wait is bounded: on expiry the CTA records an error word, its warps leave the
@@ -44,8 +48,9 @@ constexpr int kGroups = 2;                     // consumer groups taking alterna
 constexpr int kConsumers = kBlocksPerRow * kGroups;
 constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int BN = 256;                        // output columns per CTA
-constexpr int BK = 64;                         // rows of K per stage
-constexpr int kStages = 16;
+constexpr int BK = 64;                         // rows of K per block
+constexpr int kRingBlocks = 16;                // K blocks the ring holds (stages x blocks per stage)
+constexpr int kMaxStages = kRingBlocks;        // with one block per stage
 constexpr int kMaxCluster = 16;  // split-K factor: cluster sizes above 8 are non-portable
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
@@ -55,20 +60,21 @@ __device__ unsigned int g_decode_stall;  // test hook: consumers first wait on a
 
 template <int J>
 struct Layout {
-  static constexpr int kP = BK * BN / 2;        // 8 KB packed weights
-  static constexpr int kA = 8 * J * BK * 2;     // 1 KB per 8 rows of A
-  static constexpr int kS = 2 * BN * 2;         // up to two scale rows
-  static constexpr int kZ = 2 * (BN / 8) * 4;   // up to two zero-point rows
+  static constexpr int kP = BK * BN / 2;        // 8 KB packed weights per K block
+  static constexpr int kA = 8 * J * BK * 2;     // 1 KB per 8 rows of A per K block
+  static constexpr int kS = 2 * BN * 2;         // two scale rows per K block slot
+  static constexpr int kZ = 2 * (BN / 8) * 4;   // two zero-point rows per K block slot
   static constexpr int kOffP = 0;
-  static constexpr int kOffA = kOffP + kStages * kP;
-  static constexpr int kOffS = kOffA + kStages * kA;
-  static constexpr int kOffZ = kOffS + kStages * kS;
-  static constexpr int kOffBar = kOffZ + kStages * kZ;
-  static constexpr int kOffFlag = kOffBar + (2 * kStages + 1) * 8;  // + the stall-test barrier
+  static constexpr int kOffA = kOffP + kRingBlocks * kP;
+  static constexpr int kOffS = kOffA + kRingBlocks * kA;
+  static constexpr int kOffZ = kOffS + kRingBlocks * kS;
+  static constexpr int kOffBar = kOffZ + kRingBlocks * kZ;
+  // full[kMaxStages], empty[kMaxStages], the stall-test barrier
+  static constexpr int kOffFlag = kOffBar + (2 * kMaxStages + 1) * 8;
   static constexpr int kOffRed = kOffFlag + 16;                       // split-K partial tile [8J][256]
-  static constexpr int kRedBytes = 8 * J * BN * 4;
-  static constexpr int kOffGRed = kOffRed + kRedBytes;                // second group's partial tile
-  static constexpr int kUsed = kOffGRed + kRedBytes;
+  static constexpr int kOffGRed = kOffRed + 8 * J * BN * 4;           // second group's partial tile
+  static constexpr int kGRedBytes = 8 * J * BN * 4;
+  static constexpr int kUsed = kOffGRed + kGRedBytes;
   static constexpr int kSmem = kUsed + 1024;    // slack to align the base to 1024 bytes
   static_assert(kOffA % 1024 == 0 && kA % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
@@ -80,19 +86,25 @@ struct DecodeParams {
   int G;
   int zp_bias;
   int k_split;      // C: CTAs per cluster along K
-  int kb_per_cta;   // K blocks per cluster rank
+  int kb_per_cta;   // K blocks per cluster rank (a multiple of sb)
   int kb_total;     // K blocks of the problem
-  int spg;          // K blocks per scale group (>= 1)
+  int sb_shift;     // log2 of the K blocks per pipeline stage (1, 2 or 4)
+  int srows;        // scale / zero-point rows per stage
+  int g_shift;      // log2(G) when a stage spans several scale groups, else 31 (one group per stage)
 };
 
-// base + zp for nibble j of a column quad: fp16 uses 1024 (even j) and 64 (odd j, high nibble of a
-// byte, mantissa ulp 1/16); bf16 uses 128. Packed twice (both rows of a k pair).
+// Magic base of column j of a quad (see magic_quad): fp16 uses 1024 for the low nibble of a byte
+// (even j) and 64 for the high nibble (odd j, mantissa ulp 1/16); bf16 uses 128.
 template <bool BF>
-__device__ __forceinline__ uint32_t zsub_of(int j, uint32_t zp) {
-  uint32_t h;
-  if constexpr (BF) h = 0x4300u | zp;
-  else h = (j & 1) ? (0x5400u | (zp << 4)) : (0x6400u | zp);
-  return h | (h << 16);
+__device__ __forceinline__ float magic_base(int j) {
+  if constexpr (BF) return 128.f;
+  else return (j & 1) ? 64.f : 1024.f;
+}
+// A 16-bit float (fp16 or bf16 bits) widened exactly to fp32.
+template <bool BF>
+__device__ __forceinline__ float bits_to_f32(uint32_t h) {
+  if constexpr (BF) return __uint_as_float(h << 16);
+  else return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
 }
 
 // Packed (base + q) pairs of the four columns of a quad from one ldmatrix.trans register
@@ -121,7 +133,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Layout<J>;
   using T = typename DT::T;
   constexpr bool BF = DT::kBF16;
-  constexpr int kSRows = TWO_GROUPS ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -136,17 +147,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t n0 = int64_t(blockIdx.x / C) * BN;
   const int kb_begin = min(p.kb_total, rank * p.kb_per_cta);
   const int nkb = min(p.kb_total, kb_begin + p.kb_per_cta) - kb_begin;
+  const int sbs = p.sb_shift, SB = 1 << sbs;
+  const int nsts = 4 - sbs, nst = 1 << nsts;    // stages in the ring: kRingBlocks / SB
+  const int nss = (nkb + SB - 1) >> sbs;        // stages this CTA fills
 
-  const uint32_t full0 = base + L::kOffBar, empty0 = full0 + 8u * kStages;
-  const uint32_t stall_bar = empty0 + 8u * kStages;
+  const uint32_t full0 = base + L::kOffBar, empty0 = full0 + 8u * kMaxStages;
+  const uint32_t stall_bar = empty0 + 8u * kMaxStages;
   const uint32_t abort_flag = base + L::kOffFlag;
   const unsigned long long lim = g_decode_wait_limit_ns;
   const uint64_t limit_ns = lim ? lim : kDefaultWaitNs;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    // a stage is released by every consumer warp that reads a block of it: one group when a stage
+    // holds one block (the groups alternate stages), both groups otherwise
+    const uint32_t readers = SB == 1 ? kBlocksPerRow : kConsumers;
+    for (int s = 0; s < nst; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, kBlocksPerRow);  // one consumer group reads each stage
+      mbar_init(empty0 + 8u * s, readers);
     }
     mbar_init(stall_bar, 1);
     st_flag(abort_flag, 0u);
@@ -175,40 +192,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumers) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint32_t tx = L::kP + L::kA + kSRows * BN * 2 + (HAS_ZP ? kSRows * BN / 2 : 0);
-      auto load_weights = [&](int i, int s) {
-        const uint32_t full = full0 + 8u * s;
-        const int k0 = (kb_begin + i) * BK;
-        const int grow = k0 / p.G;
-        tma_load_2d(base + L::kOffP + s * L::kP, &tmP, static_cast<int>(n0 / 8), k0, full);
-        tma_load_2d(base + L::kOffS + s * L::kS, &tmS, static_cast<int>(n0), grow, full);
-        if constexpr (HAS_ZP) tma_load_2d(base + L::kOffZ + s * L::kZ, &tmZ, static_cast<int>(n0 / 8), grow, full);
+      auto stage_tx = [&](int j) {
+        const int blocks = min(SB, nkb - j * SB);
+        return static_cast<uint32_t>(SB * L::kP + blocks * L::kA + p.srows * BN * 2 +
+                                     (HAS_ZP ? p.srows * BN / 2 : 0));
       };
-      auto load_acts = [&](int i, int s) {
-        tma_load_2d(base + L::kOffA + s * L::kA, &tmA, (kb_begin + i) * BK, 0, full0 + 8u * s);
+      auto load_weights = [&](int j, int s) {
+        const uint32_t full = full0 + 8u * s;
+        const int k0 = (kb_begin + j * SB) * BK;
+        const int grow = k0 / p.G;
+        tma_load_2d(base + L::kOffP + s * SB * L::kP, &tmP, static_cast<int>(n0 / 8), k0, full);
+        tma_load_2d(base + L::kOffS + s * SB * L::kS, &tmS, static_cast<int>(n0), grow, full);
+        if constexpr (HAS_ZP)
+          tma_load_2d(base + L::kOffZ + s * SB * L::kZ, &tmZ, static_cast<int>(n0 / 8), grow, full);
+      };
+      auto load_acts = [&](int j, int s) {
+        const int blocks = min(SB, nkb - j * SB);
+        for (int b = 0; b < blocks; ++b)
+          tma_load_2d(base + L::kOffA + (s * SB + b) * L::kA, &tmA, (kb_begin + j * SB + b) * BK, 0,
+                      full0 + 8u * s);
       };
       // The packed weights, scales and zero points are model parameters that no kernel of this stream
       // writes while it runs: the first ring of them is requested before waiting for the previous
       // kernel, which overlaps their latency with its tail. The activations come after the wait.
-      const int first = nkb < kStages ? nkb : kStages;
-      for (int i = 0; i < first; ++i) {
-        mbar_arrive_expect_tx(full0 + 8u * i, tx);
-        load_weights(i, i);
+      const int first = nss < nst ? nss : nst;
+      for (int j = 0; j < first; ++j) {
+        mbar_arrive_expect_tx(full0 + 8u * j, stage_tx(j));
+        load_weights(j, j);
       }
       griddep_wait();
-      for (int i = 0; i < first; ++i) load_acts(i, i);
+      for (int j = 0; j < first; ++j) load_acts(j, j);
       int issued = first;
-      for (int i = first; i < nkb; ++i) {
-        const int s = i & (kStages - 1);
-        if (!wait_phase(empty0 + 8u * s, ((i / kStages) & 1) ^ 1u, abort_flag, limit_ns, &g_decode_error)) break;
-        mbar_arrive_expect_tx(full0 + 8u * s, tx);
-        load_weights(i, s);
-        load_acts(i, s);
-        issued = i + 1;
+      for (int j = first; j < nss; ++j) {
+        const int s = j & (nst - 1);
+        if (!wait_phase(empty0 + 8u * s, ((j >> nsts) & 1) ^ 1u, abort_flag, limit_ns, &g_decode_error)) break;
+        mbar_arrive_expect_tx(full0 + 8u * s, stage_tx(j));
+        load_weights(j, s);
+        load_acts(j, s);
+        issued = j + 1;
       }
       if (ld_flag(abort_flag)) {
-        for (int i = issued - 1; i >= 0 && i >= issued - kStages; --i)
-          drain_phase(full0 + 8u * (i & (kStages - 1)), (i / kStages) & 1, &g_decode_error);
+        for (int j = issued - 1; j >= 0 && j >= issued - nst; --j)
+          drain_phase(full0 + 8u * (j & (nst - 1)), (j >> nsts) & 1, &g_decode_error);
       }
     } else {
       griddep_wait();
@@ -226,85 +251,121 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_off = uint32_t((32 * cb + 4 * gl) * 2);
     const uint32_t z_off = uint32_t((4 * cb + (gl >> 1)) * 4);
     const int z_shift = 16 * (gl & 1);
+    constexpr int kSRows = TWO_GROUPS ? 2 : 1;  // scale groups per K block
 
-    uint32_t s2[kSRows][4], zsub[kSRows][4];
+    // Column j of this lane's quad (output column n0 + 32 cb + 4 gl + j) holds magic values base_j + q:
+    // fp16 uses 1024 for even j (low nibble of a byte) and 64 for odd j (high nibble), bf16 uses 128.
+    // zc[j] = base_j + zp and sc[j] = scale, both fp32, for the group being processed.
+    float zc[4], sc[4];
     if constexpr (!HAS_ZP) {
 #pragma unroll
-      for (int g = 0; g < kSRows; ++g)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) zsub[g][j] = zsub_of<BF>(j, static_cast<uint32_t>(p.zp_bias));
+      for (int j = 0; j < 4; ++j) zc[j] = magic_base<BF>(j) + static_cast<float>(p.zp_bias);
     }
+    const uint32_t one2 = BF ? 0x3F803F80u : 0x3C003C00u;  // (1, 1) in the activation dtype
+    const uint32_t ones[4] = {one2, one2, one2, one2};
     bool ok = true;
     if (g_decode_stall) {  // failure-detection test: a wait that can only run out
       ok = wait_phase(stall_bar, 0, abort_flag, limit_ns, &g_decode_error);
       ok = __all_sync(0xffffffffu, ok);
     }
-    for (int i = grp; i < nkb && ok; i += kGroups) {
-      const int s = i & (kStages - 1);
-      ok = wait_phase(full0 + 8u * s, (i / kStages) & 1, abort_flag, limit_ns, &g_decode_error);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      const uint32_t P = base + L::kOffP + s * L::kP;
-      const uint32_t A = base + L::kOffA + s * L::kA;
-      // this group last saw K block kb - 2: reload the scale row when a group boundary lies between
-      if (i < kGroups || (kb_begin + i) % p.spg < kGroups) {
-        const uint32_t S = base + L::kOffS + s * L::kS;
+    // Fragments of one K block: packed weights (row blocks 0..7 of column block cb), activation
+    // fragments (b0, b1 for k16 steps 0..3), raw scale and zero-point words of its group(s).
+    struct Frag {
+      uint32_t wq[8];
+      uint32_t af[J][8];
+      uint32_t sraw[kSRows][2];
+      uint32_t zraw[kSRows];
+    };
+    // Waits for K block i and loads its fragments; after this group's last block of the stage the
+    // stage is released (every value needed from it is in registers).
+    auto fetch = [&](int i, Frag &f) -> bool {
+      const int js = i >> sbs, b = i & (SB - 1);  // stage sequence number and block within the stage
+      const int s = js & (nst - 1);
+      bool w = wait_phase(full0 + 8u * s, (js >> nsts) & 1, abort_flag, limit_ns, &g_decode_error);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) return false;
+      const uint32_t P = base + L::kOffP + (s * SB + b) * L::kP;
+      const uint32_t A = base + L::kOffA + (s * SB + b) * L::kA;
+      // scale and zero-point rows of this block's group(s) within the stage's rows
+      const int r0 = (b * BK) >> p.g_shift;
+      const uint32_t S = base + L::kOffS + s * SB * L::kS + r0 * (BN * 2);
+      const uint32_t Z = base + L::kOffZ + s * SB * L::kZ + r0 * (BN / 2);
+      uint32_t r[4];
+      ldsm_x4_trans(P + p_off, r);
+      f.wq[0] = r[0]; f.wq[1] = r[1]; f.wq[2] = r[2]; f.wq[3] = r[3];
+      ldsm_x4_trans(P + p_off + 4096u, r);
+      f.wq[4] = r[0]; f.wq[5] = r[1]; f.wq[6] = r[2]; f.wq[7] = r[3];
 #pragma unroll
-        for (int g = 0; g < kSRows; ++g) {
-          uint32_t s01, s23;
-          lds64(S + g * (BN * 2) + s_off, s01, s23);
-          s2[g][0] = prmt(s01, s01, 0x1010);
-          s2[g][1] = prmt(s01, s01, 0x3232);
-          s2[g][2] = prmt(s23, s23, 0x1010);
-          s2[g][3] = prmt(s23, s23, 0x3232);
-          if constexpr (HAS_ZP) {
-            const uint32_t Z = base + L::kOffZ + s * L::kZ;
-            const uint32_t z16 = lds32(Z + g * (BN / 2) + z_off) >> z_shift;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) zsub[g][j] = zsub_of<BF>(j, (z16 >> (4 * j)) & 0xFu);
-          }
-        }
+      for (int jt = 0; jt < J; ++jt) {
+        ldsm_x4(A + jt * 1024u + a_off, r);
+        f.af[jt][0] = r[0]; f.af[jt][1] = r[1]; f.af[jt][2] = r[2]; f.af[jt][3] = r[3];
+        ldsm_x4(A + jt * 1024u + a_off2, r);
+        f.af[jt][4] = r[0]; f.af[jt][5] = r[1]; f.af[jt][6] = r[2]; f.af[jt][7] = r[3];
       }
-
-      uint32_t wq[8];        // row blocks 0..7 of column block cb
-      uint32_t af[J][8];     // B fragments: (b0, b1) for k16 steps 0..3
-      {
-        uint32_t r[4];
-        ldsm_x4_trans(P + p_off, r);
-        wq[0] = r[0]; wq[1] = r[1]; wq[2] = r[2]; wq[3] = r[3];
-        ldsm_x4_trans(P + p_off + 4096u, r);
-        wq[4] = r[0]; wq[5] = r[1]; wq[6] = r[2]; wq[7] = r[3];
 #pragma unroll
-        for (int jt = 0; jt < J; ++jt) {
-          ldsm_x4(A + jt * 1024u + a_off, r);
-          af[jt][0] = r[0]; af[jt][1] = r[1]; af[jt][2] = r[2]; af[jt][3] = r[3];
-          ldsm_x4(A + jt * 1024u + a_off2, r);
-          af[jt][4] = r[0]; af[jt][5] = r[1]; af[jt][6] = r[2]; af[jt][7] = r[3];
-        }
+      for (int g = 0; g < kSRows; ++g) {
+        lds64(S + g * (BN * 2) + s_off, f.sraw[g][0], f.sraw[g][1]);
+        if constexpr (HAS_ZP) f.zraw[g] = lds32(Z + g * (BN / 2) + z_off) >> z_shift;
       }
-      // every value this warp needs from the stage is in registers: release the stage
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8u * s);
-
+      if (lane == 0 && (((i + kGroups) >> sbs) != js || i + kGroups >= nkb)) mbar_arrive(empty0 + 8u * s);
+      return true;
+    };
+    // Exact products on the tensor core for scale group g of a block: blk = sum_k A[m,k] (base_j +
+    // q[k,n]) over the group's k16 steps, and sa = sum_k A[m,k] from the same activation fragments
+    // against ones. Then (blk - (base_j + zp) sa) = sum_k A (q - zp), and one fp32 multiply by the scale.
+    auto products = [&](const Frag &f, int g, float (&blk)[J][2][4], float (&sa)[J][4]) {
+      constexpr int kSteps = TWO_GROUPS ? 2 : 4;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int g = (TWO_GROUPS && t >= 2) ? 1 : 0;  // rows 32..63 belong to the second group
+      for (int tt = 0; tt < kSteps; ++tt) {
+        const int t = g * kSteps + tt;
         uint32_t lo[4], hi[4];
-        magic_quad<BF>(wq[2 * t], lo);
-        magic_quad<BF>(wq[2 * t + 1], hi);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          lo[j] = mul2_rn<BF>(sub2_rn<BF>(lo[j], zsub[g][j]), s2[g][j]);
-          hi[j] = mul2_rn<BF>(sub2_rn<BF>(hi[j], zsub[g][j]), s2[g][j]);
-        }
+        magic_quad<BF>(f.wq[2 * t], lo);
+        magic_quad<BF>(f.wq[2 * t + 1], hi);
         // MMA rows: g -> column 4*gl + j, g + 8 -> column 4*gl + j + 2, for j = 0 and j = 1
         const uint32_t a0[4] = {lo[0], lo[2], hi[0], hi[2]};
         const uint32_t a1[4] = {lo[1], lo[3], hi[1], hi[3]};
 #pragma unroll
         for (int jt = 0; jt < J; ++jt) {
-          mma_16816<BF>(acc[jt][0], a0, af[jt][2 * t], af[jt][2 * t + 1]);
-          mma_16816<BF>(acc[jt][1], a1, af[jt][2 * t], af[jt][2 * t + 1]);
+          if (tt == 0) {
+            mma_16816_z<BF>(blk[jt][0], a0, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
+            mma_16816_z<BF>(blk[jt][1], a1, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
+            mma_16816_z<BF>(sa[jt], ones, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
+          } else {
+            mma_16816<BF>(blk[jt][0], a0, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
+            mma_16816<BF>(blk[jt][1], a1, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
+            mma_16816<BF>(sa[jt], ones, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
+          }
         }
+      }
+    };
+    auto scale_add = [&](const Frag &f, int g, const float (&blk)[J][2][4], const float (&sa)[J][4]) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t h = (j < 2 ? f.sraw[g][0] : f.sraw[g][1]) >> (16 * (j & 1));
+        sc[j] = bits_to_f32<BF>(h & 0xFFFFu);
+        if constexpr (HAS_ZP) zc[j] = magic_base<BF>(j) + static_cast<float>((f.zraw[g] >> (4 * j)) & 0xFu);
+      }
+#pragma unroll
+      for (int jt = 0; jt < J; ++jt)
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = q + 2 * (e >> 1);  // accumulator element e of MMA q holds column j
+            const float d = fmaf(-zc[j], sa[jt][e], blk[jt][q][e]);
+            acc[jt][q][e] = fmaf(sc[j], d, acc[jt][q][e]);
+          }
+    };
+    Frag f;
+    for (int i = grp; i < nkb && ok; i += kGroups) {
+      ok = fetch(i, f);
+      if (!ok) break;
+#pragma unroll
+      for (int g = 0; g < kSRows; ++g) {
+        float blk[J][2][4], sa[J][4];
+        products(f, g, blk, sa);
+        scale_add(f, g, blk, sa);
       }
     }
   }
@@ -366,6 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
   } else {
+    // Split-K across the cluster: each rank publishes its partial tile in its own shared memory; after
+    // a cluster barrier, rank r reads slice r of every rank's tile (remote loads issued together,
+    // summed in rank order: deterministic); a second barrier keeps the tiles alive until all are read.
     float *red = reinterpret_cast<float *>(base_ptr + L::kOffRed);
     if (warp < kBlocksPerRow) {
       const int nl = 32 * warp + 4 * gl;
@@ -472,6 +536,17 @@ int64_t resident_ctas(int J, int C) {
 
 }  // namespace
 
+// Pipeline shape for a cluster rank holding `kb` K blocks: blocks per stage (bigger TMA boxes move
+// data faster, but a CTA with few blocks needs small stages to start early), and the rank's range
+// rounded up to whole stages so that every stage starts on a multiple of 64 * sb rows.
+static void rank_shape(int64_t kbt, int C, int *sb, int64_t *kb_per_cta) {
+  int64_t kb = (kbt + C - 1) / C;
+  const int b = kb >= 16 ? 4 : (kb >= 4 ? 2 : 1);
+  kb = (kb + b - 1) / b * b;
+  *sb = b;
+  *kb_per_cta = kb;
+}
+
 void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool query_device,
                       w4a16_plan_t *p) {
   (void)group_size;
@@ -482,29 +557,34 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
   // fixed latency (launch, first TMA round trip, cluster reduction) plus its K blocks; the number of
   // CTAs resident at once comes from the runtime's occupancy query (one per SM when unknown).
   constexpr double kFixedUs = 2.5, kPerBlockUs = 0.2;
-  int bestC = 1;
+  int bestC = 1, bestSB = 1;
   double best = -1.0;
-  for (int C = 1; C <= kMaxCluster; ++C) {
-    if (C > 1 && kbt < 2 * int64_t(C)) break;  // every rank keeps at least two K blocks
+  for (int Ct = 1; Ct <= kMaxCluster; ++Ct) {
+    int sb = 1;
+    int64_t kb = kbt;
+    rank_shape(kbt, Ct, &sb, &kb);
+    const int C = static_cast<int>((kbt + kb - 1) / kb);  // ranks left after rounding to whole stages
+    if (C != Ct) continue;                                 // the same plan as a smaller C
+    if (C > 1 && kb < 2) break;                            // every rank keeps at least two K blocks
     int64_t slots = query_device ? resident_ctas(J, C) : 0;
     if (slots <= 0) slots = C <= 8 ? int64_t(num_sms) / C * C : 0;
     if (slots <= 0) continue;
     const int64_t ctas = n_tiles * C;
     const int64_t waves = (ctas + slots - 1) / slots;
-    const double cost = double(waves) * (kFixedUs + kPerBlockUs * double((kbt + C - 1) / C));
+    const double cost = double(waves) * (kFixedUs + kPerBlockUs * double(kb));
     if (best < 0 || cost < best - 1e-9) {
       best = cost;
       bestC = C;
+      bestSB = sb;
     }
   }
-  const int64_t C = bestC;
   p->path = W4A16_PATH_DECODE;
-  p->words_per_lane = 1;
+  p->k_blocks_per_stage = bestSB;
   p->m_tile = 8 * J;
   p->n_tile = BN;
-  p->k_split = static_cast<int32_t>(C);
+  p->k_split = static_cast<int32_t>(bestC);
   p->warps = kConsumers + 1;
-  p->grid = n_tiles * C;
+  p->grid = n_tiles * bestC;
   p->smem_bytes = J == 1 ? Layout<1>::kSmem : Layout<2>::kSmem;
   p->stream_k = 0;
 }
@@ -516,11 +596,18 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
   const int C = pl.k_split;
   const bool zp = g.qzeros != nullptr;
   const bool two = g.group_size < BK && g.group_size != g.K;  // G = 32: two groups per K block
-  const int srows = two ? 2 : 1;
+  const int64_t kbt = (g.K + BK - 1) / BK;
+  int sb = 1;
+  int64_t kb_per_cta = kbt;
+  rank_shape(kbt, C, &sb, &kb_per_cta);
+  if (sb != pl.k_blocks_per_stage || (kbt + kb_per_cta - 1) / kb_per_cta != C) return cudaErrorInvalidValue;
+  // scale / zero-point rows per stage: the groups of 64 * sb rows (G in {32, 64, 128} divides that
+  // when it is smaller; a larger G, or G = K, leaves one group per stage)
+  const int srows = g.group_size < BK * sb ? BK * sb / g.group_size : 1;
   const int64_t NW = g.N / 8, ng = g.K / g.group_size;
   CUtensorMap tA, tP, tS, tZ;
   if (!tma_encode_2d(&tA, 2, g.a, g.K, g.M, g.K * 2, BK, 8 * J, true) ||
-      !tma_encode_2d(&tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK, true) ||
+      !tma_encode_2d(&tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK * sb, true) ||
       !tma_encode_2d(&tS, 2, g.scales, g.N, ng, g.N * 2, BN, srows, false))
     return cudaErrorInvalidValue;
   if (zp) {
@@ -555,9 +642,12 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
   prm.G = g.group_size;
   prm.zp_bias = g.zp_bias;
   prm.k_split = C;
-  prm.kb_total = static_cast<int>((g.K + BK - 1) / BK);
-  prm.kb_per_cta = (prm.kb_total + C - 1) / C;
-  prm.spg = g.group_size >= BK ? g.group_size / BK : 1;
+  prm.kb_total = static_cast<int>(kbt);
+  prm.kb_per_cta = static_cast<int>(kb_per_cta);
+  prm.sb_shift = sb == 4 ? 2 : (sb == 2 ? 1 : 0);
+  prm.srows = srows;
+  // a stage of 64 * sb rows spans several groups only for G in {32, 64, 128} below that size
+  prm.g_shift = g.group_size < BK * sb ? (g.group_size == 32 ? 5 : (g.group_size == 64 ? 6 : 7)) : 31;
 
   const int64_t n_tiles = (g.N + BN - 1) / BN;
   cudaLaunchConfig_t cfg = {};

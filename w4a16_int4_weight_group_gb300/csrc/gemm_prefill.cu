@@ -535,6 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // Warps 0 and 1 ran their roles on lane 0 only: reconverge each warp before the block-wide barrier,
+  // so that no lane reaches it ahead of its warp (the barrier counts warps) and TMEM is released only
+  // after every epilogue warp has read its accumulators.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -607,7 +611,7 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
     tiles = ((M + 255) / 256) * n_tiles;
   }
   p->path = W4A16_PATH_PREFILL;
-  p->words_per_lane = 1;
+  p->k_blocks_per_stage = 1;
   p->m_tile = 128 * MT;
   p->n_tile = BN;
   p->k_split = 1;
