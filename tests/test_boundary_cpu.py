@@ -121,6 +121,21 @@ def test_dispatcher_decode_for_small_m_and_split_k(w):
     assert w.w4a16_plan(1, 2560, 19456, 128, 0, True, 76)["grid"] <= 152
 
 
+def test_prefill_plan_stream_k_only_when_whole_tiles_leave_sms_idle(w):
+    # the prefill workload: N = 34816 fills the SMs in whole waves, N = 5120 does not
+    for m in (512, 1024, 4096):
+        p = w.w4a16_plan(m, 5120, 34816, 64, 1, True, 152)
+        assert p["path_name"] == "prefill" and p["stream_k"] == 0 and p["grid"] == (m // 256) * 136, p
+        q = w.w4a16_plan(m, 17408, 5120, 64, 1, True, 152)
+        assert q["stream_k"] == 1 and q["m_tile"] == 256 and q["grid"] == 152, q
+        # without a workspace the same call runs one CTA per tile
+        r = w.w4a16_plan(m, 17408, 5120, 64, 1, True, 152, with_workspace=False)
+        assert r["stream_k"] == 0
+    # few tiles: fewer CTAs than SMs, so that the owner's fix-up stays short
+    p = w.w4a16_plan(256, 4096, 1024, 32, 1, True, 152)
+    assert p["stream_k"] == 1 and 4 < p["grid"] < 64, p
+
+
 def test_dispatcher_uses_runtime_m_not_a_frozen_config(w):
     # the same layer, decode and prefill sizes, in any order: plans depend only on the runtime M
     k, n, g = 5120, 7168, 128

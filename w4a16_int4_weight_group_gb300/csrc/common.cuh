@@ -227,6 +227,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tensor_map
       : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Orders this thread's earlier generic-proxy view of global memory (e.g. after an acquire of data
+// other CTAs wrote) before its later async-proxy (bulk copy) reads of it.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+// Bulk copy of `bytes` contiguous bytes (16-byte aligned, a multiple of 16) from global into shared
+// memory, completion counted on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 
 // Bounded wait on an mbarrier phase. On expiry it sets the CTA's abort flag (a shared-memory word
 // at `abort_flag`) and ORs 1 into the kernel's device error word; it also returns false early once

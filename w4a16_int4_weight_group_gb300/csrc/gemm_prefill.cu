@@ -60,7 +60,12 @@ struct PLayout {
   static constexpr int kOffS = kOffP + SA * kPBytes;
   static constexpr int kOffZ = kOffS + SA * kSBytes;
   static constexpr int kOffBar = kOffZ + SA * kZBytes;
-  static constexpr int kNumBars = 2 * SA + 2 * SB + 4;  // + accumulator full/empty, epilogue done, stall test
+  // stream-K fix-up: after the last MMA the A and B stage buffers stage contributors' partial tiles,
+  // 32 KB chunks (one epilogue column chunk of all eight warps)
+  static constexpr int kFixChunk = 32768;
+  static constexpr int kFixSlots = (kOffP - kOffA) / kFixChunk;
+  // + accumulator full/empty, epilogue done, stall test, fix-up ready, fix-up slot full/empty
+  static constexpr int kNumBars = 2 * SA + 2 * SB + 5 + 2 * kFixSlots;
   static constexpr int kOffSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffFlag = kOffSlot + 4;
   static constexpr int kSmemUsed = kOffFlag + 4;
@@ -197,6 +202,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_units = static_cast<int>(u_end - u_begin);
   const int64_t t_first = u_begin / nk;
   const int kb_first = static_cast<int>(u_begin - t_first * nk);
+  // The share's last segment needs a fix-up when it starts a tile (K block 0) but ends inside it: the
+  // CTAs after this one hold the rest of that tile and publish their partial tiles.
+  const int64_t t_last = n_units > 0 ? (u_end - 1) / nk : t_first;
+  const bool fix_needed = n_units > 0 && (t_last > t_first || kb_first == 0) && u_end < (t_last + 1) * nk;
+  int64_t c_fix = blockIdx.x;  // last CTA holding part of tile t_last
+  if (fix_needed)
+    while (c_fix + 1 < G && unit_begin(c_fix + 1, total, G) < (t_last + 1) * nk) ++c_fix;
+  const int n_con = static_cast<int>(c_fix - blockIdx.x);  // contributors to add
 
   const uint32_t bar0 = base + kOffBar;
   auto full_a = [&](int s) { return bar0 + 8u * s; };
@@ -207,6 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t accum_empty = accum_full + 8u;
   const uint32_t epi_done = accum_empty + 8u;  // the epilogue warps' stores of a split tile are done
   const uint32_t stall_bar = epi_done + 8u;
+  const uint32_t fix_ready = stall_bar + 8u;  // committed after this CTA's last MMA
+  constexpr int kFixSlots = L::kFixSlots;
+  auto fix_full = [&](int s) { return fix_ready + 8u * (1 + s); };
+  auto fix_empty = [&](int s) { return fix_ready + 8u * (1 + kFixSlots + s); };
   const uint32_t abort_flag = base + kOffFlag;
   const uint32_t slot = base + kOffSlot;
 
@@ -226,6 +243,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(accum_empty, kDequantWarps);
     mbar_init(epi_done, kDequantWarps);
     mbar_init(stall_bar, 1);
+    mbar_init(fix_ready, 1);
+    for (int s = 0; s < kFixSlots; ++s) {
+      mbar_init(fix_full(s), 1);
+      mbar_init(fix_empty(s), kDequantWarps);
+    }
     st_flag(abort_flag, 0u);
     mbar_init_fence();
   }
@@ -277,6 +299,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ld_flag(abort_flag)) {
         // let this CTA's own copies land before its shared memory is released
         for (int i = issued - 1; i >= 0 && i >= issued - SA; --i) drain_phase(full_a(i % SA), (i / SA) & 1, &g_prefill_error);
+      } else if (fix_needed) {
+        // Fix-up loader: once the last MMA is done the stage buffers are free; wait for each
+        // contributor's "partial ready" flag, then stream their partial tiles, chunk by chunk in
+        // the order the epilogue adds them (column chunk major, CTA order within a chunk).
+        bool ok = wait_phase(fix_ready, 0, abort_flag, limit_ns, &g_prefill_error);
+        const uint64_t t0 = globaltimer();
+        for (int64_t cc = int64_t(blockIdx.x) + 1; cc <= c_fix && ok; ++cc) {
+          while (ld_acquire_u32(p.flags + cc) == 0u) {
+            if (ld_flag(abort_flag) || globaltimer() - t0 > limit_ns) {
+              st_flag(abort_flag, 1u);
+              atomicOr(&g_prefill_error, 1u);
+              ok = false;
+              break;
+            }
+          }
+        }
+        fence_proxy_async_all();  // the partials were written by other CTAs' generic stores
+        const int n_chunks = 4 * MT * n_con;
+        int fix_issued = 0;
+        for (int n = 0; n < n_chunks && ok; ++n) {
+          const int sl = n % kFixSlots;
+          if (n >= kFixSlots)
+            ok = wait_phase(fix_empty(sl), ((n / kFixSlots) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error);
+          if (!ok) break;
+          const int it = n / n_con;
+          const int64_t cc = int64_t(blockIdx.x) + 1 + (n - it * n_con);
+          const float *src = p.partials + (cc * (4 * MT) + it) * (L::kFixChunk / 4);
+          mbar_arrive_expect_tx(fix_full(sl), L::kFixChunk);
+          bulk_load(base + kOffA + sl * L::kFixChunk, src, L::kFixChunk, fix_full(sl));
+          fix_issued = n + 1;
+        }
+        if (!ok) {
+          for (int n = fix_issued - 1; n >= 0 && n >= fix_issued - kFixSlots; --n)
+            drain_phase(fix_full(n % kFixSlots), (n / kFixSlots) & 1, &g_prefill_error);
+        }
       }
     }
   } else if (warp == 1) {
@@ -332,6 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         umma_commit(accum_full);
         drain_phase(accum_full, seg & 1, &g_prefill_error);
+      } else {
+        umma_commit(fix_ready);  // every MMA of this CTA is done: its stage buffers are free
       }
     }
   } else {
@@ -416,28 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool whole = owner && kb == nk - 1;
         const int64_t m0 = (t % p.m_tiles) * BM;
         const int64_t n0 = (t / p.m_tiles) * BN;
-        // CTAs whose share starts inside this tile after this one: they hold the rest of it
-        int64_t c_last = blockIdx.x;
-        if (owner && !whole) {
-          while (c_last + 1 < G && unit_begin(c_last + 1, total, G) < (t + 1) * nk) ++c_last;
-          // wait until each of them has published its partial tile (one poller per warp)
-          for (int64_t cc = blockIdx.x + 1; cc <= c_last && ok; ++cc) {
-            if (lane == 0) {
-              const uint64_t t0 = globaltimer();
-              while (ld_acquire_u32(p.flags + cc) == 0u) {
-                if (ld_flag(abort_flag)) { ok = false; break; }
-                if (globaltimer() - t0 > limit_ns) {
-                  st_flag(abort_flag, 1u);
-                  atomicOr(&g_prefill_error, 1u);
-                  ok = false;
-                  break;
-                }
-              }
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            __syncwarp();  // orders lane 0's acquire before every lane's reads of the partial tile
-          }
-        }
+        // CTAs whose share starts inside this tile after this one hold the rest of it. A tile owned
+        // without its end is always this CTA's last segment: the producer thread stages the
+        // contributors' partial tiles (fix-up loader) once all MMAs are done.
+        const int64_t c_last = (owner && !whole) ? c_fix : int64_t(blockIdx.x);
 #pragma unroll 1
         for (int it = 0; it < 4 * MT; ++it) {
           const int mt = it >> 2, ch = it & 3;  // accumulator (row half of the tile) and 32-column chunk
@@ -451,6 +492,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
           }
           if (!ok) continue;
+          // partial tiles travel in accumulator order: chunk `it` of a CTA is 32 KB, float4 j of
+          // thread (dw, lane) at ((dw * 8 + j) * 32 + lane) * 16 bytes (a warp's float4 j is 512
+          // contiguous bytes)
+          const uint32_t lane_off = uint32_t((dw * 8 * 32 + lane) * 16);
+          if (!owner) {
+            // publish this CTA's partial tile
+            float4 *dst = reinterpret_cast<float4 *>(p.partials + (int64_t(blockIdx.x) * (4 * MT) + it) * (L::kFixChunk / 4)) +
+                          lane_off / 16;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[32 * j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            continue;
+          }
+          if (!whole) {
+            // add the contributors' chunks in CTA order (deterministic), as the loader stages them
+            for (int cci = 0; cci < n_con && ok; ++cci) {
+              const int n = it * n_con + cci;
+              const int sl = n % kFixSlots;
+              ok = wait_phase(fix_full(sl), (n / kFixSlots) & 1, abort_flag, limit_ns, &g_prefill_error);
+              ok = __all_sync(0xffffffffu, ok);
+              if (!ok) break;
+              const uint32_t src = base + kOffA + sl * L::kFixChunk + lane_off;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint32_t x0, x1, x2, x3;
+                lds128(src + 512u * j, x0, x1, x2, x3);
+                r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + __uint_as_float(x0));
+                r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + __uint_as_float(x1));
+                r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + __uint_as_float(x2));
+                r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + __uint_as_float(x3));
+              }
+              __syncwarp();
+              if (lane == 0) mbar_arrive(fix_empty(sl));
+            }
+            if (!ok) continue;
+          }
 #pragma unroll
           for (int g8 = 0; g8 < 4; ++g8) {
             // accumulator columns hold outputs n+0, n+4, n+1, n+5, n+2, n+6, n+3, n+7
@@ -464,20 +542,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[3] = __uint_as_float(r[8 * g8 + 6]);
             v[7] = __uint_as_float(r[8 * g8 + 7]);
             const int tc = col0 + 8 * g8;  // column within the tile
-            if (!owner) {
-              // publish this CTA's partial tile (row-major fp32 [BM][BN])
-              float4 *dst = reinterpret_cast<float4 *>(p.partials + (int64_t(blockIdx.x) * BM + tr) * BN + tc);
-              dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-              dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-              continue;
-            }
-            // owner: add the partials of the following CTAs in order (deterministic), then store
-            for (int64_t cc = int64_t(blockIdx.x) + 1; cc <= c_last; ++cc) {
-              const float4 *src = reinterpret_cast<const float4 *>(p.partials + (cc * BM + tr) * BN + tc);
-              const float4 a0 = __ldcg(src), a1 = __ldcg(src + 1);  // L2: written by another SM
-              v[0] += a0.x; v[1] += a0.y; v[2] += a0.z; v[3] += a0.w;
-              v[4] += a1.x; v[5] += a1.y; v[6] += a1.z; v[7] += a1.w;
-            }
             const int64_t n = n0 + tc;
             if (!row_ok || n >= p.N) continue;
             if (p.bias) {
@@ -586,29 +650,44 @@ size_t prefill_workspace_bytes(int64_t M, int64_t K, int64_t N, int group_size, 
 void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool workspace,
                        w4a16_plan_t *p) {
   (void)group_size;
-  // One CTA per SM (shared memory). Two 128-row accumulators halve the dequantisation work per
-  // FLOP, which makes a tile-row about 1.4x cheaper (measured); pick the smaller waves x work.
+  // Cost in units of one (256-row tile, K block) step of the two-accumulator kernel. One CTA per SM.
+  //  * one CTA per tile: waves x K blocks; a 128-row step costs 0.7 (dequantisation is not halved);
+  //  * stream-K over G CTAs (MT = 2, needs the workspace): an even share of all steps per CTA, plus
+  //    the owner's fix-up, ~2 steps per contributor whose partial tile it adds (a 256 KB read).
   const int64_t n_tiles = (N + BN - 1) / BN;
   const int64_t nk = (K + BK - 1) / BK;
-  double best_cost = -1.0;
-  int MT = 1;
+  const int64_t sms = std::max(1, num_sms);
+  double best = -1.0;
+  int MT = 2;
+  int64_t grid = 0;
+  bool stream_k = false;
   for (int mt = 2; mt >= 1; --mt) {
     const int64_t tiles = ((M + 128 * mt - 1) / (128 * mt)) * n_tiles;
-    const double cost = double((tiles + num_sms - 1) / num_sms) * mt * (mt == 1 ? 1.4 : 1.0);
-    if (best_cost < 0 || cost < best_cost - 1e-9) {
-      best_cost = cost;
+    const double cost = double((tiles + sms - 1) / sms) * double(nk) * (mt == 1 ? 0.7 : 1.0);
+    if (best < 0 || cost < best - 1e-9) {
+      best = cost;
       MT = mt;
+      grid = tiles;
     }
   }
-  int64_t tiles = ((M + 128 * MT - 1) / (128 * MT)) * n_tiles;
-  const int64_t waves = (tiles + num_sms - 1) / num_sms;
-  const double fill = double(tiles) / double(waves * num_sms);
-  // Stream-K when whole tiles leave SMs idle in the last wave and a workspace is available: every SM
-  // gets the same number of (tile, K block) units. Two accumulators then always pay off.
-  const bool stream_k = workspace && fill < 0.85 && M > 128;
-  if (stream_k) {
-    MT = 2;
-    tiles = ((M + 255) / 256) * n_tiles;
+  // Stream-K only when whole tiles leave SMs idle in the last wave: with full waves, the CTAs of a
+  // wave share A row tiles and weight column tiles in L2, which stream-K's spread of tiles loses.
+  const int64_t waves = (grid + sms - 1) / sms;
+  const double fill = double(grid) / double(waves * sms);
+  const int64_t tiles2 = ((M + 255) / 256) * n_tiles;
+  if (workspace && M > 128 && fill < 0.85) {
+    const int64_t total = tiles2 * nk;
+    for (int64_t g = 1; g <= std::min<int64_t>(sms, total); ++g) {
+      const int64_t share = (total + g - 1) / g;
+      const int64_t parts = (g + tiles2 - 1) / tiles2 + 1;  // CTAs touching one tile, at most
+      const double cost = double(share) + 2.0 * double(parts - 1);
+      if (cost < best - 1e-9) {
+        best = cost;
+        MT = 2;
+        grid = g;
+        stream_k = true;
+      }
+    }
   }
   p->path = W4A16_PATH_PREFILL;
   p->k_blocks_per_stage = 1;
@@ -616,7 +695,7 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
   p->n_tile = BN;
   p->k_split = 1;
   p->warps = kThreads / 32;
-  p->grid = stream_k ? std::min<int64_t>(num_sms, tiles * nk) : tiles;
+  p->grid = grid;
   p->smem_bytes = smem_of(MT);
   p->stream_k = stream_k ? 1 : 0;
 }
