@@ -88,7 +88,6 @@ struct DecodeParams {
   int k_split;      // C: CTAs per cluster along K
   int kb_per_cta;   // K blocks per cluster rank (a multiple of sb)
   int kb_total;     // K blocks of the problem
-  int sb_shift;     // log2 of the K blocks per pipeline stage (1, 2 or 4)
   int srows;        // scale / zero-point rows per stage
   int g_shift;      // log2(G) when a stage spans several scale groups, else 31 (one group per stage)
 };
@@ -125,7 +124,7 @@ __device__ __forceinline__ void magic_quad(uint32_t w, uint32_t (&h)[4]) {
   }
 }
 
-template <class DT, int J, bool HAS_ZP, bool TWO_GROUPS>
+template <class DT, int J, bool HAS_ZP, bool TWO_GROUPS, int SBS>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmP,
                   const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ,
@@ -147,8 +146,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t n0 = int64_t(blockIdx.x / C) * BN;
   const int kb_begin = min(p.kb_total, rank * p.kb_per_cta);
   const int nkb = min(p.kb_total, kb_begin + p.kb_per_cta) - kb_begin;
-  const int sbs = p.sb_shift, SB = 1 << sbs;
-  const int nsts = 4 - sbs, nst = 1 << nsts;    // stages in the ring: kRingBlocks / SB
+  // K blocks per stage (1, 2 or 4) and stages in the ring, both compile-time (runtime shifts here
+  // cost more than the whole per-block index arithmetic they replace)
+  constexpr int sbs = SBS, SB = 1 << SBS;
+  constexpr int nsts = 4 - SBS, nst = 1 << nsts;
   const int nss = (nkb + SB - 1) >> sbs;        // stages this CTA fills
 
   const uint32_t full0 = base + L::kOffBar, empty0 = full0 + 8u * kMaxStages;
@@ -474,14 +475,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                           const DecodeParams);
 
-template <class DT, int J>
+template <class DT, int J, int SBS>
 KernelFn pick_zg(bool zp, bool two) {
-  if (zp) return two ? decode_kernel<DT, J, true, true> : decode_kernel<DT, J, true, false>;
-  return two ? decode_kernel<DT, J, false, true> : decode_kernel<DT, J, false, false>;
+  if (zp) return two ? decode_kernel<DT, J, true, true, SBS> : decode_kernel<DT, J, true, false, SBS>;
+  return two ? decode_kernel<DT, J, false, true, SBS> : decode_kernel<DT, J, false, false, SBS>;
 }
-KernelFn pick(int dtype, int J, bool zp, bool two) {
-  if (dtype == W4A16_BF16) return J == 1 ? pick_zg<BF16, 1>(zp, two) : pick_zg<BF16, 2>(zp, two);
-  return J == 1 ? pick_zg<F16, 1>(zp, two) : pick_zg<F16, 2>(zp, two);
+template <class DT, int SBS>
+KernelFn pick_j(int J, bool zp, bool two) {
+  return J == 1 ? pick_zg<DT, 1, SBS>(zp, two) : pick_zg<DT, 2, SBS>(zp, two);
+}
+template <class DT>
+KernelFn pick_dt(int J, bool zp, bool two, int sb) {
+  if (sb == 4) return pick_j<DT, 2>(J, zp, two);
+  if (sb == 2) return pick_j<DT, 1>(J, zp, two);
+  return pick_j<DT, 0>(J, zp, two);
+}
+KernelFn pick(int dtype, int J, bool zp, bool two, int sb) {
+  return dtype == W4A16_BF16 ? pick_dt<BF16>(J, zp, two, sb) : pick_dt<F16>(J, zp, two, sb);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -501,7 +511,7 @@ int64_t resident_ctas(int J, int C) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
   if (!have[dev][J - 1][C]) {
-    const KernelFn fn = pick(W4A16_F16, J, true, false);
+    const KernelFn fn = pick(W4A16_F16, J, true, false, 1);  // occupancy does not depend on the stage size
     const int smem = J == 1 ? Layout<1>::kSmem : Layout<2>::kSmem;
     int n = 0;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
@@ -541,7 +551,7 @@ int64_t resident_ctas(int J, int C) {
 // rounded up to whole stages so that every stage starts on a multiple of 64 * sb rows.
 static void rank_shape(int64_t kbt, int C, int *sb, int64_t *kb_per_cta) {
   int64_t kb = (kbt + C - 1) / C;
-  const int b = kb >= 16 ? 4 : (kb >= 4 ? 2 : 1);
+  const int b = kb >= 16 ? 4 : 1;  // two-block stages measured slower than one-block ones here
   kb = (kb + b - 1) / b * b;
   *sb = b;
   *kb_per_cta = kb;
@@ -615,16 +625,16 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
   } else {
     tZ = tP;  // unused
   }
-  const KernelFn fn = pick(g.dtype, J, zp, two);
+  const KernelFn fn = pick(g.dtype, J, zp, two, sb);
   const int smem = J == 1 ? Layout<1>::kSmem : Layout<2>::kSmem;
   {
     static std::mutex mu;
-    static bool configured[64][2][2][2][2] = {};
+    static bool configured[64][2][2][2][2][3] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
-    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][J - 1][zp][two];
+    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][J - 1][zp][two][sb == 4 ? 2 : sb - 1];
     if (!done) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
@@ -644,7 +654,6 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
   prm.k_split = C;
   prm.kb_total = static_cast<int>(kbt);
   prm.kb_per_cta = static_cast<int>(kb_per_cta);
-  prm.sb_shift = sb == 4 ? 2 : (sb == 2 ? 1 : 0);
   prm.srows = srows;
   // a stage of 64 * sb rows spans several groups only for G in {32, 64, 128} below that size
   prm.g_shift = g.group_size < BK * sb ? (g.group_size == 32 ? 5 : (g.group_size == 64 ? 6 : 7)) : 31;
