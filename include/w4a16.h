@@ -144,8 +144,10 @@ w4a16_status w4a16_gemm(const void *a, const int32_t *b_q, const void *scales, c
  * output tiles do not fill the GPU in whole waves use stream-K: persistent CTAs take equal shares of
  * the (tile, K block) work and exchange fp32 partial tiles through the workspace.
  *   workspace       device memory, 256-byte aligned, at least w4a16_gemm_workspace_size(...) bytes
- *                   (a smaller or NULL workspace simply disables stream-K); it must be zero-filled
- *                   before its first use, and every call leaves it zero-filled again
+ *                   (a smaller or NULL workspace simply disables stream-K). Its first 4 KiB hold
+ *                   per-CTA flags: they must be zero before the first use, and every call leaves
+ *                   them zero again; the rest is scratch whose contents between calls do not matter
+ *                   (zero-filling the whole buffer once is the simple way to satisfy this)
  *   workspace_bytes its size
  * Calls that may run concurrently (different streams) need different workspaces. Everything else
  * is as for w4a16_gemm (no allocation, no synchronisation, no host read).

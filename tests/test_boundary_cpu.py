@@ -133,7 +133,12 @@ def test_prefill_plan_stream_k_only_when_whole_tiles_leave_sms_idle(w):
         assert r["stream_k"] == 0
     # few tiles: fewer CTAs than SMs, so that the owner's fix-up stays short
     p = w.w4a16_plan(256, 4096, 1024, 32, 1, True, 152)
-    assert p["stream_k"] == 1 and 4 < p["grid"] < 64, p
+    assert p["stream_k"] == 1 and 4 < p["grid"] < 152, p
+    # mid M (17..128): 128-row tiles leave most SMs idle; stream-K over 128-row tiles fills them
+    for m in (17, 32, 64, 128):
+        p = w.w4a16_plan(m, 5120, 7168, 128, 1, False, 152)
+        assert p["path_name"] == "prefill" and p["stream_k"] == 1 and p["m_tile"] == 128, (m, p)
+        assert p["grid"] >= 100, (m, p)
 
 
 def test_dispatcher_uses_runtime_m_not_a_frozen_config(w):

@@ -220,11 +220,12 @@ def test_sweep_shapes_sampled(w, M, K, N, G):
 
 
 @pytest.mark.parametrize("M,K,N,G,dt,asym", [(512, 4096, 1024, 128, "bf16", True), (300, 2048, 768, 64, "f16", False),
-                                           (1024, 17408, 5120, 64, "bf16", True), (256, 4096, 1024, 32, "bf16", True)])
+                                           (1024, 17408, 5120, 64, "bf16", True), (256, 4096, 1024, 32, "bf16", True),
+                                           (40, 5120, 7168, 128, "f16", True)])
 def test_stream_k_matches_oracle_and_leaves_workspace_clean(w, M, K, N, G, dt, asym):
     """Persistent stream-K prefill: several CTAs share each output tile through the workspace; the
-    tile's owner stages their partial tiles in rounds through its shared memory (the last case has
-    five contributors per tile, more chunks than staging slots, and two scale groups per K block)."""
+    tile's owner stages their partial tiles in rounds through its shared memory (more chunks than
+    staging slots; 256-row and 128-row tiles; two scale groups per K block; a mid-M case)."""
     c = synth.make_case(M, K, N, G, dt, asym=asym, bias=True, seed=M + K)
     code = 1 if dt == "bf16" else 0
     plan = w.w4a16_plan(M, K, N, G, code, asym, 0, with_workspace=True)
@@ -243,7 +244,7 @@ def test_stream_k_matches_oracle_and_leaves_workspace_clean(w, M, K, N, G, dt, a
         outs.append(torch_to_bits(out))
     assert np.array_equal(outs[0], outs[1]), "stream-K must be deterministic"
     grid = plan["grid"]
-    flags = ws[grid * plan["m_tile"] * 256 * 4: grid * plan["m_tile"] * 256 * 4 + grid * 4]
+    flags = ws[:grid * 4]  # the flag area opens the workspace
     assert int(flags.count_nonzero()) == 0, "flags must be left zero"
     rng = np.random.default_rng(M)
     rows = sorted({0, M - 1} | set(rng.integers(0, M, size=6).tolist()))

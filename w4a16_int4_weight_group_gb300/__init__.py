@@ -167,9 +167,10 @@ _workspaces = {}
 
 
 def workspace_for(device: torch.device, stream, nbytes: int) -> torch.Tensor:
-    """A zero-filled scratch buffer of at least nbytes, kept per (device, stream) and grown on demand.
+    """A scratch buffer of at least nbytes, kept per (device, stream) and grown on demand.
 
-    The library leaves it zero-filled after every call, so it is zeroed only when (re)allocated.
+    It is zero-filled when (re)allocated; the library leaves its flag area (the first 4 KiB) zero
+    after every call and needs nothing else of the rest between calls.
     """
     key = (device.index, int(stream))
     buf = _workspaces.get(key)

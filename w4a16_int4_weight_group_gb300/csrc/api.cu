@@ -371,8 +371,8 @@ w4a16_status w4a16_gemm_noalloc(const void *a, const int32_t *b_q, const void *s
     w4a16_plan_t plan;
     choose_plan(g, dev.num_sms, tma_available(), /*query_device=*/true, /*workspace=*/true, &plan);
     if (plan.path == W4A16_PATH_PREFILL && plan.stream_k) {
-      const size_t flags_at = static_cast<size_t>(plan.grid) * plan.m_tile * plan.n_tile * sizeof(float);
-      e = cudaMemsetAsync(static_cast<uint8_t *>(scratch) + flags_at, 0, static_cast<size_t>(plan.grid) * 4,
+      // the flags sit at the start of the scratch (one word per CTA)
+      e = cudaMemsetAsync(scratch, 0, static_cast<size_t>(plan.grid) * 4,
                           g.stream);
       if (e != cudaSuccess) return cuda_fail(e, "clear static scratch flags");
     }

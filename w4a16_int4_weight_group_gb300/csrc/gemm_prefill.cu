@@ -75,6 +75,10 @@ struct PLayout {
 };
 
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+// Stream-K workspace: the per-CTA "partial ready" flags first, at a fixed place (so that no plan's
+// partial tiles ever cover another plan's flags), then one fp32 partial tile per CTA.
+constexpr size_t kFlagBytes = 4096;
+constexpr int64_t kMaxStreamKCtas = kFlagBytes / 4;
 
 __device__ unsigned int g_prefill_error;
 __device__ unsigned long long g_wait_limit_ns;
@@ -643,8 +647,8 @@ size_t prefill_workspace_bytes(int64_t M, int64_t K, int64_t N, int group_size, 
   w4a16_plan_t pl;
   prefill_make_plan(M, K, N, group_size, num_sms, /*workspace=*/true, &pl);
   if (!pl.stream_k) return 0;
-  // one fp32 partial tile and one flag per CTA
-  return static_cast<size_t>(pl.grid) * pl.m_tile * BN * sizeof(float) + static_cast<size_t>(pl.grid) * 4 + 256;
+  // the flag area, then one fp32 partial tile per CTA
+  return kFlagBytes + static_cast<size_t>(pl.grid) * pl.m_tile * BN * sizeof(float);
 }
 
 void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool workspace,
@@ -652,8 +656,9 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
   (void)group_size;
   // Cost in units of one (256-row tile, K block) step of the two-accumulator kernel. One CTA per SM.
   //  * one CTA per tile: waves x K blocks; a 128-row step costs 0.7 (dequantisation is not halved);
-  //  * stream-K over G CTAs (MT = 2, needs the workspace): an even share of all steps per CTA, plus
-  //    the owner's fix-up, ~2 steps per contributor whose partial tile it adds (a 256 KB read).
+  //  * stream-K over G CTAs (needs the workspace): an even share of all steps per CTA, plus the
+  //    owner's fix-up, ~2 steps per contributor whose partial tile it adds (a 256 KB read; half that
+  //    for 128-row tiles).
   const int64_t n_tiles = (N + BN - 1) / BN;
   const int64_t nk = (K + BK - 1) / BK;
   const int64_t sms = std::max(1, num_sms);
@@ -672,20 +677,24 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
   }
   // Stream-K only when whole tiles leave SMs idle in the last wave: with full waves, the CTAs of a
   // wave share A row tiles and weight column tiles in L2, which stream-K's spread of tiles loses.
+  // Both tile heights are considered (128-row steps cost 0.7, and a contributor's partial tile half).
   const int64_t waves = (grid + sms - 1) / sms;
   const double fill = double(grid) / double(waves * sms);
-  const int64_t tiles2 = ((M + 255) / 256) * n_tiles;
-  if (workspace && M > 128 && fill < 0.85) {
-    const int64_t total = tiles2 * nk;
-    for (int64_t g = 1; g <= std::min<int64_t>(sms, total); ++g) {
-      const int64_t share = (total + g - 1) / g;
-      const int64_t parts = (g + tiles2 - 1) / tiles2 + 1;  // CTAs touching one tile, at most
-      const double cost = double(share) + 2.0 * double(parts - 1);
-      if (cost < best - 1e-9) {
-        best = cost;
-        MT = 2;
-        grid = g;
-        stream_k = true;
+  if (workspace && fill < 0.85) {
+    for (int mt = 2; mt >= 1; --mt) {
+      const int64_t tiles = ((M + 128 * mt - 1) / (128 * mt)) * n_tiles;
+      const int64_t total = tiles * nk;
+      const double step = mt == 1 ? 0.7 : 1.0, fix = mt == 1 ? 1.0 : 2.0;
+      for (int64_t g = 1; g <= std::min<int64_t>(std::min<int64_t>(sms, kMaxStreamKCtas), total); ++g) {
+        const int64_t share = (total + g - 1) / g;
+        const int64_t parts = (g + tiles - 1) / tiles + 1;  // CTAs touching one tile, at most
+        const double cost = double(share) * step + fix * double(parts - 1);
+        if (cost < best - 1e-9) {
+          best = cost;
+          MT = mt;
+          grid = g;
+          stream_k = true;
+        }
       }
     }
   }
@@ -738,11 +747,12 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl) {
   prm.partials = nullptr;
   prm.flags = nullptr;
   if (pl.stream_k) {
-    // workspace: [grid][BM][BN] fp32 partial tiles, then [grid] flags (zero between calls)
+    // workspace: the flag area (zero between calls), then [grid][BM][BN] fp32 partial tiles
     const size_t part_bytes = static_cast<size_t>(pl.grid) * BM * BN * sizeof(float);
-    if (!g.workspace || g.workspace_bytes < part_bytes + static_cast<size_t>(pl.grid) * 4) return cudaErrorInvalidValue;
-    prm.partials = static_cast<float *>(g.workspace);
-    prm.flags = reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(g.workspace) + part_bytes);
+    if (!g.workspace || pl.grid > kMaxStreamKCtas || g.workspace_bytes < kFlagBytes + part_bytes)
+      return cudaErrorInvalidValue;
+    prm.flags = static_cast<unsigned int *>(g.workspace);
+    prm.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(g.workspace) + kFlagBytes);
   }
   prm.bias = static_cast<const uint16_t *>(g.bias);
   prm.out = static_cast<uint16_t *>(g.out);
