@@ -96,6 +96,23 @@ def scale_units(name, x):
     return x / 1e12 if name == "prefill" else x / 1e9
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of the ranks' values (each rank passes its own); x itself on one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(name: str, units_per_step: float, steps: int, world: int, elapsed_ms: float) -> float:
+    """Aggregate throughput: the units every rank processed (weak scaling: the same workload per
+    rank) over the slowest rank's time."""
+    return scale_units(name, units_per_step * steps * world) / (elapsed_ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(HERE, "MEASURED_PEAKS.json")
     try:
@@ -310,14 +327,9 @@ def run_cuda(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     barrier()
     clk = clocks.stop()
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     units_per_step = sum(c["units"] for c in calls)
-    total_units = units_per_step * args.steps * world
-    value = scale_units(name, total_units) / (elapsed_ms / 1e3)
+    value = whole_job_value(name, units_per_step, args.steps, world, elapsed_ms)
     launches = int(round(launches_per_step * args.steps))
 
     # ---- end to end through the public API with host buffers (eager, copies inside) ----
@@ -332,12 +344,8 @@ def run_cuda(args, rank, world, local_rank):
         e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = scale_units(name, units_per_step * e2e_steps * world) / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = whole_job_value(name, units_per_step, e2e_steps, world, e2e_ms)
     h2d = a_dev.numel() * a_dev.element_size()
     d2h = o_dev.numel() * o_dev.element_size()
 
