@@ -121,11 +121,13 @@ def test_dispatcher_decode_for_small_m_and_split_k(w):
     assert w.w4a16_plan(1, 2560, 19456, 128, 0, True, 76)["grid"] <= 152
 
 
-def test_prefill_plan_stream_k_only_when_whole_tiles_leave_sms_idle(w):
-    # the prefill workload: N = 34816 fills the SMs in whole waves, N = 5120 does not
+def test_prefill_plan_stream_k_with_a_workspace(w):
+    # the prefill workload: persistent stream-K CTAs, one per SM, 256-row tiles
     for m in (512, 1024, 4096):
         p = w.w4a16_plan(m, 5120, 34816, 64, 1, True, 152)
-        assert p["path_name"] == "prefill" and p["stream_k"] == 0 and p["grid"] == (m // 256) * 136, p
+        assert p["path_name"] == "prefill" and p["stream_k"] == 1 and p["grid"] == 152, p
+        p = w.w4a16_plan(m, 5120, 34816, 64, 1, True, 152, with_workspace=False)
+        assert p["stream_k"] == 0 and p["grid"] == (m // 256) * 136, p
         q = w.w4a16_plan(m, 17408, 5120, 64, 1, True, 152)
         assert q["stream_k"] == 1 and q["m_tile"] == 256 and q["grid"] == 152, q
         # without a workspace the same call runs one CTA per tile
@@ -134,7 +136,7 @@ def test_prefill_plan_stream_k_only_when_whole_tiles_leave_sms_idle(w):
     # few tiles: fewer CTAs than SMs, so that the owner's fix-up stays short
     p = w.w4a16_plan(256, 4096, 1024, 32, 1, True, 152)
     assert p["stream_k"] == 1 and 4 < p["grid"] < 152, p
-    # mid M (17..128): 128-row tiles leave most SMs idle; stream-K over 128-row tiles fills them
+    # mid M (17..128): 128-row tiles would leave most SMs idle; stream-K over 128-row tiles fills them
     for m in (17, 32, 64, 128):
         p = w.w4a16_plan(m, 5120, 7168, 128, 1, False, 152)
         assert p["path_name"] == "prefill" and p["stream_k"] == 1 and p["m_tile"] == 128, (m, p)

@@ -675,12 +675,10 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
       grid = tiles;
     }
   }
-  // Stream-K only when whole tiles leave SMs idle in the last wave: with full waves, the CTAs of a
-  // wave share A row tiles and weight column tiles in L2, which stream-K's spread of tiles loses.
-  // Both tile heights are considered (128-row steps cost 0.7, and a contributor's partial tile half).
-  const int64_t waves = (grid + sms - 1) / sms;
-  const double fill = double(grid) / double(waves * sms);
-  if (workspace && fill < 0.85) {
+  // Stream-K over both tile heights (128-row steps cost 0.7, and a contributor's partial tile half).
+  // Even when whole tiles fill every wave, the persistent CTAs measured equal or faster (they skip
+  // the per-tile launch, prologue and pipeline fill), so the cost model alone decides.
+  if (workspace) {
     for (int mt = 2; mt >= 1; --mt) {
       const int64_t tiles = ((M + 128 * mt - 1) / (128 * mt)) * n_tiles;
       const int64_t total = tiles * nk;
