@@ -253,3 +253,21 @@ def test_stream_k_matches_oracle_and_leaves_workspace_clean(w, M, K, N, G, dt, a
     out2 = w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"], use_workspace=False)
     torch.cuda.synchronize()
     check_against_oracle(c, torch_to_bits(out2), rows=rows, cols=sample_cols(N, rng, k=64), label="no workspace")
+
+
+@pytest.mark.parametrize("shift", [0, 8])
+def test_prefill_output_alignment_paths(w, shift):
+    """32-byte stores when `out` is 32-byte aligned, 16-byte stores when it is only 16-byte aligned
+    (an output slice 8 elements into a buffer): the same values either way."""
+    M, K, N, G = 300, 2048, 768, 64
+    c = synth.make_case(M, K, N, G, "bf16", asym=True, bias=True, seed=77)
+    t = case_tensors(c)
+    big = torch.empty(M * N + 16, dtype=t["a"].dtype, device="cuda")
+    out = big[shift:shift + M * N].view(M, N)
+    assert out.data_ptr() % 32 == (0 if shift == 0 else 16)
+    w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"], out=out)
+    torch.cuda.synchronize()
+    assert w.w4a16_plan(M, K, N, G, 1, True, 0)["path_name"] == "prefill"
+    rng = np.random.default_rng(shift)
+    check_against_oracle(c, torch_to_bits(out), rows=np.arange(0, M, 13), cols=sample_cols(N, rng, k=64),
+                         label=f"out shifted by {shift}")

@@ -119,6 +119,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32-byte global store (sm_100+ vector width), 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&o)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]),
+               "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+               : "memory");
+}
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -533,42 +539,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) continue;
           }
+          // Two 8-column groups at a time: 16 outputs = 32 bytes per store (a whole sector of the
+          // row) when the rows and the output pointer are 32-byte aligned; 16-byte stores otherwise.
+          const bool wide = (p.N & 15) == 0 && (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
 #pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8) {
-            // accumulator columns hold outputs n+0, n+4, n+1, n+5, n+2, n+6, n+3, n+7
-            float v[8];
-            v[0] = __uint_as_float(r[8 * g8 + 0]);
-            v[4] = __uint_as_float(r[8 * g8 + 1]);
-            v[1] = __uint_as_float(r[8 * g8 + 2]);
-            v[5] = __uint_as_float(r[8 * g8 + 3]);
-            v[2] = __uint_as_float(r[8 * g8 + 4]);
-            v[6] = __uint_as_float(r[8 * g8 + 5]);
-            v[3] = __uint_as_float(r[8 * g8 + 6]);
-            v[7] = __uint_as_float(r[8 * g8 + 7]);
-            const int tc = col0 + 8 * g8;  // column within the tile
-            const int64_t n = n0 + tc;
-            if (!row_ok || n >= p.N) continue;
-            if (p.bias) {
-              const uint4 bv = *reinterpret_cast<const uint4 *>(p.bias + n);
-              const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+          for (int gp = 0; gp < 2 && row_ok; ++gp) {
+            uint32_t o[8];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int g8 = 2 * gp + h;
+              // accumulator columns hold outputs n+0, n+4, n+1, n+5, n+2, n+6, n+3, n+7
+              float v[8];
+              v[0] = __uint_as_float(r[8 * g8 + 0]);
+              v[4] = __uint_as_float(r[8 * g8 + 1]);
+              v[1] = __uint_as_float(r[8 * g8 + 2]);
+              v[5] = __uint_as_float(r[8 * g8 + 3]);
+              v[2] = __uint_as_float(r[8 * g8 + 4]);
+              v[6] = __uint_as_float(r[8 * g8 + 5]);
+              v[3] = __uint_as_float(r[8 * g8 + 6]);
+              v[7] = __uint_as_float(r[8 * g8 + 7]);
+              const int64_t n = n0 + col0 + 8 * g8;
+              if (p.bias && n < p.N) {
+                const uint4 bv = *reinterpret_cast<const uint4 *>(p.bias + n);
+                const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  v[2 * e] += bits_to_float(static_cast<uint16_t>(bw[e] & 0xFFFFu), BF);
+                  v[2 * e + 1] += bits_to_float(static_cast<uint16_t>(bw[e] >> 16), BF);
+                }
+              }
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                v[2 * e] += bits_to_float(static_cast<uint16_t>(bw[e] & 0xFFFFu), BF);
-                v[2 * e + 1] += bits_to_float(static_cast<uint16_t>(bw[e] >> 16), BF);
+                if constexpr (BF) {
+                  const __nv_bfloat162 tt = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                  o[4 * h + e] = *reinterpret_cast<const uint32_t *>(&tt);
+                } else {
+                  const __half2 tt = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
+                  o[4 * h + e] = *reinterpret_cast<const uint32_t *>(&tt);
+                }
               }
             }
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if constexpr (BF) {
-                const __nv_bfloat162 tt = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-                o[e] = *reinterpret_cast<const uint32_t *>(&tt);
-              } else {
-                const __half2 tt = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
-                o[e] = *reinterpret_cast<const uint32_t *>(&tt);
-              }
+            const int64_t n = n0 + col0 + 16 * gp;  // first of the 16 columns
+            uint16_t *dst = p.out + m * p.N + n;
+            if (wide && n + 16 <= p.N) {
+              st_global_v8(dst, o);
+            } else {
+              if (n < p.N) *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+              if (n + 8 < p.N) *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(o[4], o[5], o[6], o[7]);
             }
-            *reinterpret_cast<uint4 *>(p.out + m * p.N + n) = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
         // the accumulators have been read: the next segment's MMAs may overwrite them
