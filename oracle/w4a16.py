@@ -74,6 +74,21 @@ def unpack(packed: np.ndarray, n: Optional[int] = None, cols: Optional[Sequence[
     return ((words >> shifts) & np.uint64(0xF)).astype(np.uint8)
 
 
+def pack_k(q: np.ndarray) -> np.ndarray:
+    """uint8 [K, N] -> int32 [N, K/8], packed along K (the PR #40977 report's "[N, K//8] int32"
+    layout): word c of row n = sum_j q[8c + j, n] << 4j. The order inside a word is not printed;
+    sequential little-endian along K is the reading taken (the same convention as ``pack``)."""
+    q = np.asarray(q)
+    if q.ndim != 2 or q.shape[0] % 8:
+        raise ValueError("q must be [K, N] with K % 8 == 0")
+    return pack(q.T)
+
+
+def unpack_k(k_packed: np.ndarray) -> np.ndarray:
+    """int32 [N, K/8] -> uint8 [K, N]; the inverse of ``pack_k``."""
+    return unpack(k_packed).T.copy()
+
+
 # ----------------------------------------------------------------------------------------------
 # dequantisation
 # ----------------------------------------------------------------------------------------------
@@ -170,6 +185,6 @@ def fp64_eps_bound(K: int) -> float:
     return 1e-12 * max(1, K)
 
 
-__all__ = ["pack", "unpack", "zero_points", "dequant_exact", "dequant_t", "gemm_ref",
+__all__ = ["pack", "unpack", "pack_k", "unpack_k", "zero_points", "dequant_exact", "dequant_t", "gemm_ref",
            "weight_rounding_bound", "out_t", "tolerance", "within_tolerance", "TOLERANCE",
            "SUPPORTED_GROUP_SIZES", "t_unit_roundoff", "t_min_subnormal"]

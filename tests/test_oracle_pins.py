@@ -445,3 +445,30 @@ def test_mutant_rounding_mode_is_caught(monkeypatch):
 
     monkeypatch.setattr(ieee, "t_encode_rne", round_half_up)
     assert not _runs_clean(lambda: test_encode_ties_and_near_ties_match_library("f16"))
+
+
+# ----------------------------------------------------------------------------------------------
+# packing along K (the [N, K/8] layout of the PR #40977 report)
+# ----------------------------------------------------------------------------------------------
+def test_pack_k_hand_words():
+    # q[k, n] = (k + 2n) % 16 on an 8 x 8 block. Row n of the K-packed tensor holds k = 0..7 of
+    # column n, nibble j = k: n = 0 -> 0,1,...,7 = 0x76543210; n = 1 -> 2..9 = 0x98765432;
+    # n = 7 -> 14,15,0,1,...,5 = 0x543210FE (worked by hand).
+    q = np.array([[(k + 2 * n) % 16 for n in range(8)] for k in range(8)], dtype=np.uint8)
+    kp = oracle.pack_k(q).view(np.uint32)
+    assert kp.shape == (8, 1)
+    assert int(kp[0, 0]) == 0x76543210
+    assert int(kp[1, 0]) == 0x98765432
+    assert int(kp[7, 0]) == 0x543210FE
+
+
+def test_pack_k_round_trip_and_relation_to_n_packing():
+    rng = np.random.default_rng(5)
+    q = rng.integers(0, 16, size=(24, 40), dtype=np.uint8)
+    kp = oracle.pack_k(q)
+    assert kp.shape == (40, 3)
+    assert np.array_equal(oracle.unpack_k(kp), q)
+    # the same weights in the two layouts: unpacking either gives the same matrix
+    assert np.array_equal(oracle.unpack(oracle.pack(q)), oracle.unpack_k(kp))
+    # the layouts really differ: the first K-packed word holds column 0, rows 0..7
+    assert int(kp.view(np.uint32)[0, 0]) == sum(int(q[k, 0]) << (4 * k) for k in range(8))
