@@ -104,11 +104,25 @@ w4a16_status w4a16_unpack(const int32_t *packed, uint8_t *q, int64_t rows, int64
                           w4a16_stream_t stream);
 
 /*
+ * w4a16_repack_k_to_n - ingest weights packed along K, int32 [n, k/8] (the "[N, K//8] int32" layout
+ * of the PR #40977 report, implementation breakdown and key source snippets), into this library's
+ * b_q int32 [k, n/8] layout. The report does not print the order of the nibbles inside a K-packed
+ * word; this function reads nibble j (bits 4j..4j+3) of word c of row r as weight [k = 8c+j, n = r],
+ * the same sequential little-endian convention as w4a16_pack, applied along K. A load-time step.
+ *   k_packed: device, int32 [n, k/8];  b_q: device, int32 [k, n/8].
+ * Errors: INVALID_ARG if k or n is not positive or not divisible by 8, a pointer is NULL, or the
+ * buffers overlap; MISALIGNED if either is not 4-byte aligned.
+ */
+w4a16_status w4a16_repack_k_to_n(const int32_t *k_packed, int32_t *b_q, int64_t k, int64_t n,
+                                 w4a16_stream_t stream);
+
+/*
  * w4a16_dequant - materialise dequant(W) in the activation dtype:
  *   w_out[k, n] = RNE_dtype((q[k, n] - zp[k/G, n]) * scales[k/G, n])
- * i.e. the exact product rounded once to nearest-even. These are exactly the values the GEMM
- * kernels feed to their multiply-accumulate (dequantisation rule: PR #40977 report, key source
- * snippets, test reference; zp = qzeros nibble, or zp_bias when qzeros is NULL).
+ * i.e. the exact product rounded once to nearest-even (dequantisation rule: PR #40977 report, key
+ * source snippets, test reference; zp = qzeros nibble, or zp_bias when qzeros is NULL). The prefill
+ * kernel feeds exactly these values to its tensor-core MMA; the decode kernel multiplies the exact
+ * integers and applies the scale in fp32, so a one-hot activation row reproduces them exactly too.
  *   b_q [k, n/8] int32, scales [k/G, n] dtype, qzeros [k/G, n/8] int32 or NULL, w_out [k, n] dtype.
  * Errors: as w4a16_gemm's validation (dtype, n % 8, group size, k % G, zp_bias, nulls, overlap).
  */

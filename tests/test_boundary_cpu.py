@@ -163,3 +163,14 @@ def test_dispatcher_generic_for_unaligned_shapes(w):
 def test_plan_rejects_bad_config(w):
     with pytest.raises(w.W4A16Error):
         w.w4a16_plan(4, 256, 516, 128, 0, False, 152)
+
+
+def test_repack_k_to_n_validation(w):
+    import ctypes
+    L = w.lib()
+    p0, p1 = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000)
+    assert L.w4a16_repack_k_to_n(p0, p1, 12, 16, None) == 1            # k % 8
+    assert L.w4a16_repack_k_to_n(p0, p1, 16, 12, None) == 1            # n % 8
+    assert L.w4a16_repack_k_to_n(None, p1, 16, 16, None) == 1          # null
+    assert L.w4a16_repack_k_to_n(ctypes.c_void_p(0x10002), p1, 16, 16, None) == 3  # misaligned
+    assert L.w4a16_repack_k_to_n(p0, ctypes.c_void_p(0x10010), 16, 16, None) == 1  # overlap

@@ -208,9 +208,11 @@ def test_prefill_workload_sampled(w, args):
     check_against_oracle(c, out, rows=rows, cols=cols, label="prefill sampled")
 
 
-@pytest.mark.parametrize("M,K,N,G", [(1024, 5120, 7168, 128), (256, 17408, 512, 17408)])
+@pytest.mark.parametrize("M,K,N,G", [(1024, 5120, 7168, 128), (256, 17408, 512, 17408), (24, 5120, 7168, 128),
+                                     (64, 17408, 5120, 17408), (16, 5120, 34816, 128)])
 def test_sweep_shapes_sampled(w, M, K, N, G):
-    """27B-class layer shapes of the M sweep, per-group and per-channel scales."""
+    """27B-class layer shapes of the M sweep, per-group and per-channel scales; the mid-M sizes run
+    stream-K over 128-row tiles, M = 16 the two-accumulator-set decode kernel."""
     for dt, asym in (("f16", False), ("bf16", True)):
         c = synth.make_case(M, K, N, G, dt, asym=asym, seed=M + G)
         out = run(w, c)
@@ -271,3 +273,16 @@ def test_prefill_output_alignment_paths(w, shift):
     rng = np.random.default_rng(shift)
     check_against_oracle(c, torch_to_bits(out), rows=np.arange(0, M, 13), cols=sample_cols(N, rng, k=64),
                          label=f"out shifted by {shift}")
+
+
+@pytest.mark.parametrize("K,N", [(8, 8), (2112, 1152), (1152, 4224), (4104, 264)])
+def test_repack_k_to_n_bitexact(w, K, N):
+    """K-packed [N, K/8] words -> b_q [K, N/8]: bit-exact against the oracle's unpack-along-K then
+    pack-along-N (including K, N not multiples of 64)."""
+    rng = np.random.default_rng(K + N)
+    kp = rng.integers(0, 2 ** 32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    got = w.w4a16_repack_k_to_n(torch.from_numpy(kp).cuda())
+    torch.cuda.synchronize()
+    want = oracle.pack(oracle.unpack_k(kp))
+    assert np.array_equal(got.cpu().numpy(), want)
+

@@ -49,6 +49,7 @@ _c_i64, _c_int, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
 SIGNATURES = [
     ("w4a16_pack", _c_int, [_vp, _vp, _c_i64, _c_i64, _vp]),
     ("w4a16_unpack", _c_int, [_vp, _vp, _c_i64, _c_i64, _vp]),
+    ("w4a16_repack_k_to_n", _c_int, [_vp, _vp, _c_i64, _c_i64, _vp]),
     ("w4a16_dequant", _c_int, [_vp, _vp, _vp, _c_i64, _c_i64, _c_int, _c_int, _c_int, _vp, _vp]),
     ("w4a16_gemm", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_int, _vp]),
     ("w4a16_gemm_ws", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_int, _vp,
@@ -148,6 +149,19 @@ def w4a16_unpack(packed: torch.Tensor, n: Optional[int] = None, q: Optional[torc
     dev = _require_cuda(q, packed)
     _check(lib().w4a16_unpack(_ptr(packed), _ptr(q), rows, n, _stream(dev)))
     return q
+
+
+def w4a16_repack_k_to_n(k_packed: torch.Tensor, b_q: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Weights packed along K, int32 [n, k/8] -> this library's b_q, int32 [k, n/8] (nibble j of a
+    K-packed word is row 8c+j; see the C header)."""
+    if k_packed.dtype != torch.int32 or k_packed.dim() != 2:
+        raise ValueError("k_packed must be a 2-D int32 tensor")
+    n, k = k_packed.shape[0], k_packed.shape[1] * 8
+    if b_q is None:
+        b_q = torch.empty((k, n // 8), dtype=torch.int32, device=k_packed.device)
+    dev = _require_cuda(k_packed, b_q)
+    _check(lib().w4a16_repack_k_to_n(_ptr(k_packed), _ptr(b_q), k, n, _stream(dev)))
+    return b_q
 
 
 def w4a16_dequant(b_q: torch.Tensor, scales: torch.Tensor, qzeros: Optional[torch.Tensor], group_size: int,

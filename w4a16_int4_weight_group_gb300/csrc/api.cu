@@ -252,6 +252,21 @@ w4a16_status w4a16_unpack(const int32_t *packed, uint8_t *q, int64_t rows, int64
   return ok();
 }
 
+w4a16_status w4a16_repack_k_to_n(const int32_t *k_packed, int32_t *b_q, int64_t k, int64_t n,
+                                 w4a16_stream_t stream) {
+  if (k <= 0 || n <= 0 || k >= kMaxDim || n >= kMaxDim)
+    return fail(W4A16_ERR_INVALID_ARG, "k (%lld) and n (%lld) must be > 0", (long long)k, (long long)n);
+  if (k % 8 || n % 8)
+    return fail(W4A16_ERR_INVALID_ARG, "k (%lld) and n (%lld) must be divisible by 8", (long long)k, (long long)n);
+  if (!k_packed || !b_q) return fail(W4A16_ERR_INVALID_ARG, "k_packed and b_q must not be NULL");
+  if (!aligned(k_packed, 4) || !aligned(b_q, 4)) return fail(W4A16_ERR_MISALIGNED, "k_packed and b_q must be 4-byte aligned");
+  if (overlaps(range(k_packed, k * n / 2), range(b_q, k * n / 2)))
+    return fail(W4A16_ERR_INVALID_ARG, "k_packed and b_q overlap");
+  const cudaError_t e = launch_repack_k_to_n(k_packed, b_q, k, n, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "w4a16_repack_k_to_n launch");
+  return ok();
+}
+
 w4a16_status w4a16_dequant(const int32_t *b_q, const void *scales, const int32_t *qzeros, int64_t k,
                            int64_t n, int group_size, int zp_bias, w4a16_dtype dtype, void *w_out,
                            w4a16_stream_t stream) {

@@ -47,6 +47,7 @@ bool tma_available();
 
 cudaError_t launch_pack(const uint8_t *q, int32_t *packed, int64_t rows, int64_t n, cudaStream_t s);
 cudaError_t launch_unpack(const int32_t *packed, uint8_t *q, int64_t rows, int64_t n, cudaStream_t s);
+cudaError_t launch_repack_k_to_n(const int32_t *k_packed, int32_t *b_q, int64_t k, int64_t n, cudaStream_t s);
 cudaError_t launch_dequant(const int32_t *b_q, const void *scales, const int32_t *qzeros, int64_t k,
                            int64_t n, int group_size, int zp_bias, int dtype, void *w_out,
                            cudaStream_t s);

@@ -41,6 +41,29 @@ __global__ void unpack_kernel(const int32_t *__restrict__ packed, uint8_t *__res
   }
 }
 
+// [N, K/8] -> [K, N/8]: one thread per 8x8 block of 4-bit values; it reads the eight K-packed words
+// of columns 8bn..8bn+7 (word c: rows 8c..8c+7) and writes the eight N-packed words of rows
+// 8c..8c+7 (word bn: columns 8bn..8bn+7), consecutive threads writing consecutive words.
+__global__ void repack_k_to_n_kernel(const int32_t *__restrict__ kp, int32_t *__restrict__ np, int64_t K,
+                                     int64_t N) {
+  const int64_t kw = K / 8, nw = N / 8;
+  const int64_t blocks = kw * nw;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < blocks;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t c = i / nw, bn = i - c * nw;
+    uint32_t in[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) in[t] = static_cast<uint32_t>(kp[(8 * bn + t) * kw + c]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) w |= ((in[t] >> (4 * j)) & 0xFu) << (4 * t);
+      np[(8 * c + j) * nw + bn] = static_cast<int32_t>(w);
+    }
+  }
+}
+
 template <class DT>
 __global__ void dequant_kernel(const int32_t *__restrict__ b_q, const uint16_t *__restrict__ scales,
                                const int32_t *__restrict__ qzeros, int64_t K, int64_t N, int G,
@@ -80,6 +103,14 @@ cudaError_t launch_unpack(const int32_t *packed, uint8_t *q, int64_t rows, int64
   const int64_t words = rows * (n / 8);
   if (words == 0) return cudaSuccess;
   unpack_kernel<<<grid_for(words), kThreads, 0, s>>>(packed, q, words);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_k_to_n(const int32_t *k_packed, int32_t *b_q, int64_t k, int64_t n, cudaStream_t s) {
+  const int64_t blocks = (k / 8) * (n / 8);
+  if (blocks == 0) return cudaSuccess;
+  repack_k_to_n_kernel<<<grid_for(blocks), kThreads, 0, s>>>(k_packed, b_q, k, n);
   note_launch();
   return cudaGetLastError();
 }
