@@ -106,7 +106,14 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(device: torch.device):
+    """The current CUDA stream of `device` as a raw handle (without building a Stream object when
+    the runtime offers the raw query)."""
+    if _raw_stream is not None:
+        return ctypes.c_void_p(_raw_stream(device.index if device.index is not None else torch.cuda.current_device()))
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
@@ -180,6 +187,10 @@ def w4a16_dequant(b_q: torch.Tensor, scales: torch.Tensor, qzeros: Optional[torc
 _workspaces = {}
 
 
+# workspace bytes per (device, m, k, n, group_size, dtype): a pure function of the shape and the device
+_ws_need: dict = {}
+
+
 def workspace_for(device: torch.device, stream, nbytes: int) -> torch.Tensor:
     """A scratch buffer of at least nbytes, kept per (device, stream) and grown on demand.
 
@@ -217,15 +228,21 @@ def w4a16_gemm(a: torch.Tensor, b_q: torch.Tensor, scales: torch.Tensor, qzeros:
     if b_q.dtype != torch.int32 or (qzeros is not None and qzeros.dtype != torch.int32):
         raise ValueError("b_q and qzeros must be int32")
     stream = _stream(dev)
-    need = int(lib().w4a16_gemm_workspace_size(m, k, n, group_size, _dtype_code(a.dtype))) if use_workspace else 0
+    code = _dtype_code(a.dtype)
+    need = 0
+    if use_workspace:
+        key = (dev.index, m, k, n, group_size, code)
+        need = _ws_need.get(key)
+        if need is None:
+            need = _ws_need[key] = int(lib().w4a16_gemm_workspace_size(m, k, n, group_size, code))
     if need:
         ws = workspace_for(dev, stream.value or 0, need)
         _check(lib().w4a16_gemm_ws(_ptr(a), _ptr(b_q), _ptr(scales), _ptr(qzeros), group_size, zp_bias,
-                                   _ptr(bias), _ptr(out), m, k, n, _dtype_code(a.dtype), _ptr(ws), ws.numel(),
+                                   _ptr(bias), _ptr(out), m, k, n, code, _ptr(ws), ws.numel(),
                                    stream))
     else:
         _check(lib().w4a16_gemm(_ptr(a), _ptr(b_q), _ptr(scales), _ptr(qzeros), group_size, zp_bias, _ptr(bias),
-                                _ptr(out), m, k, n, _dtype_code(a.dtype), stream))
+                                _ptr(out), m, k, n, code, stream))
     return out
 
 

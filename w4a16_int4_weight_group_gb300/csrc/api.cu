@@ -318,12 +318,11 @@ static w4a16_status gemm_impl(GemmArgs &g) {
   cudaError_t e = current_device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "device query");
   w4a16_plan_t plan;
-  bool ws = false;
-  if (g.workspace) {
-    const size_t need = prefill_workspace_bytes(g.M, g.K, g.N, g.group_size, dev.num_sms);
-    ws = need > 0 && g.workspace_bytes >= need;
-  }
-  choose_plan(g, dev.num_sms, tma_available(), /*query_device=*/true, ws, &plan);
+  const bool tma = tma_available();
+  choose_plan(g, dev.num_sms, tma, /*query_device=*/true, g.workspace != nullptr, &plan);
+  // a stream-K plan whose workspace the caller did not provide in full falls back to whole tiles
+  if (g.workspace && g.workspace_bytes < prefill_plan_workspace_bytes(plan))
+    choose_plan(g, dev.num_sms, tma, /*query_device=*/true, /*workspace=*/false, &plan);
   switch (plan.path) {
     case W4A16_PATH_DECODE: e = launch_gemm_decode(g, plan); break;
     case W4A16_PATH_PREFILL: e = launch_gemm_prefill(g, plan); break;
@@ -376,21 +375,19 @@ w4a16_status w4a16_gemm_noalloc(const void *a, const int32_t *b_q, const void *s
   size_t scratch_bytes = 0;
   e = prefill_static_scratch(&scratch, &scratch_bytes);
   if (e != cudaSuccess) return cuda_fail(e, "static scratch address (cudaGetSymbolAddress)");
-  const size_t need = prefill_workspace_bytes(m, k, n, group_size, dev.num_sms);
+  // the plan this call will run (gemm_impl makes the same choice); only stream-K needs scratch
+  w4a16_plan_t plan;
+  choose_plan(g, dev.num_sms, tma_available(), /*query_device=*/true, /*workspace=*/true, &plan);
+  const size_t need = prefill_plan_workspace_bytes(plan);
   if (need > scratch_bytes)
     return fail(W4A16_ERR_UNSUPPORTED,
                 "this call needs %zu bytes of scratch (stream-K over %d SMs); the static scratch holds %zu",
                 need, dev.num_sms, scratch_bytes);
   if (need > 0) {
-    // The array keeps the previous call's contents: the stream-K flags must start at zero.
-    w4a16_plan_t plan;
-    choose_plan(g, dev.num_sms, tma_available(), /*query_device=*/true, /*workspace=*/true, &plan);
-    if (plan.path == W4A16_PATH_PREFILL && plan.stream_k) {
-      // the flags sit at the start of the scratch (one word per CTA)
-      e = cudaMemsetAsync(scratch, 0, static_cast<size_t>(plan.grid) * 4,
-                          g.stream);
-      if (e != cudaSuccess) return cuda_fail(e, "clear static scratch flags");
-    }
+    // The array keeps the previous call's contents: the stream-K flags (one word per CTA at the
+    // start of the scratch) must start at zero.
+    e = cudaMemsetAsync(scratch, 0, static_cast<size_t>(plan.grid) * 4, g.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clear static scratch flags");
   }
   g.workspace = scratch;
   g.workspace_bytes = scratch_bytes;
@@ -398,10 +395,17 @@ w4a16_status w4a16_gemm_noalloc(const void *a, const int32_t *b_q, const void *s
 }
 
 size_t w4a16_gemm_workspace_size(int64_t m, int64_t k, int64_t n, int group_size, int dtype) {
-  if (check_config(k, n, group_size, dtype) != W4A16_OK || m <= 0) return 0;
+  if (check_config(k, n, group_size, dtype) != W4A16_OK || m <= 0 || m >= kMaxDim) return 0;
   DeviceInfo dev;
   if (current_device_info(&dev) != cudaSuccess) return 0;
-  return prefill_workspace_bytes(m, k, n, group_size, dev.num_sms);
+  // the dispatcher's own choice (16-byte aligned tensors assumed): decode shapes need none
+  static const int32_t kAlignedWord[4] = {0, 0, 0, 0};
+  const void *p16 = reinterpret_cast<const void *>((reinterpret_cast<uintptr_t>(kAlignedWord) + 15) & ~uintptr_t(15));
+  GemmArgs g{p16, static_cast<const int32_t *>(p16), p16, nullptr, group_size, 8, nullptr, const_cast<void *>(p16),
+             m, k, n, dtype, nullptr};
+  w4a16_plan_t plan;
+  choose_plan(g, dev.num_sms, /*tma=*/true, /*query_device=*/true, /*workspace=*/true, &plan);
+  return prefill_plan_workspace_bytes(plan);
 }
 
 w4a16_status w4a16_plan(int64_t m, int64_t k, int64_t n, int group_size, int dtype, int has_zp,

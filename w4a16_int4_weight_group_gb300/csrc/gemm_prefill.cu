@@ -661,12 +661,16 @@ bool prefill_supported(const GemmArgs &g) {
          tiles <= 0x7fffffff;
 }
 
+size_t prefill_plan_workspace_bytes(const w4a16_plan_t &pl) {
+  if (pl.path != W4A16_PATH_PREFILL || !pl.stream_k) return 0;
+  // the flag area, then one fp32 partial tile per CTA
+  return kFlagBytes + static_cast<size_t>(pl.grid) * pl.m_tile * BN * sizeof(float);
+}
+
 size_t prefill_workspace_bytes(int64_t M, int64_t K, int64_t N, int group_size, int num_sms) {
   w4a16_plan_t pl;
   prefill_make_plan(M, K, N, group_size, num_sms, /*workspace=*/true, &pl);
-  if (!pl.stream_k) return 0;
-  // the flag area, then one fp32 partial tile per CTA
-  return kFlagBytes + static_cast<size_t>(pl.grid) * pl.m_tile * BN * sizeof(float);
+  return prefill_plan_workspace_bytes(pl);
 }
 
 void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool workspace,

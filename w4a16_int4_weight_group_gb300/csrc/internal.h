@@ -70,6 +70,8 @@ bool prefill_supported(const GemmArgs &g);
 void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool workspace,
                        w4a16_plan_t *p);
 size_t prefill_workspace_bytes(int64_t M, int64_t K, int64_t N, int group_size, int num_sms);
+// Workspace bytes a prefill plan needs (0 unless it is stream-K).
+size_t prefill_plan_workspace_bytes(const w4a16_plan_t &plan);
 // Device address and size of the library's static scratch array on the current device (looked up
 // once per device).
 cudaError_t prefill_static_scratch(void **ptr, size_t *bytes);
