@@ -241,6 +241,11 @@ def run_cuda(args, rank, world, local_rank):
                       "scales": [sc] + [sc.clone() for _ in range(reps - 1)],
                       "qzeros": None if qz is None else [qz] + [qz.clone() for _ in range(reps - 1)],
                       "bias": bi, "reps": reps, "G": G}
+        pool = pools[key]
+        # one prepared layer per weight replica (the public API a model would hold per layer)
+        pool["layers"] = [w4.W4A16Linear(pool["b_q"][r], pool["scales"][r],
+                                         None if qz is None else pool["qzeros"][r], G, 8, bi)
+                          for r in range(reps)]
     # Activations and outputs of all the calls of a step live in one device buffer each (16-byte
     # aligned slices), mirrored by one pinned host buffer each: the end-to-end leg moves a step's
     # inputs with one host-to-device copy and its results with one device-to-host copy.
@@ -274,9 +279,7 @@ def run_cuda(args, rank, world, local_rank):
             pool = pools[c["key"]]
             r = counters[c["key"]] % pool["reps"]
             counters[c["key"]] += 1
-            w4.w4a16_gemm(c["a"], pool["b_q"][r], pool["scales"][r],
-                          None if pool["qzeros"] is None else pool["qzeros"][r], pool["G"], 8, pool["bias"],
-                          out=c["out"])
+            pool["layers"][r](c["a"], out=c["out"])
         if use_host:
             o_pin.copy_(o_dev, non_blocking=True)
 

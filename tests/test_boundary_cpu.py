@@ -174,3 +174,13 @@ def test_repack_k_to_n_validation(w):
     assert L.w4a16_repack_k_to_n(None, p1, 16, 16, None) == 1          # null
     assert L.w4a16_repack_k_to_n(ctypes.c_void_p(0x10002), p1, 16, 16, None) == 3  # misaligned
     assert L.w4a16_repack_k_to_n(p0, ctypes.c_void_p(0x10010), 16, 16, None) == 1  # overlap
+
+
+def test_prepared_layer_rejects_host_tensors(w):
+    import torch
+    b_q = torch.zeros((256, 64), dtype=torch.int32)
+    scales = torch.zeros((2, 512), dtype=torch.float16)
+    with pytest.raises(ValueError):
+        w.W4A16Linear(b_q, scales, None, 128)
+    with pytest.raises(ValueError):
+        w.W4A16Linear(b_q.to(torch.int64), scales, None, 128)

@@ -286,3 +286,17 @@ def test_repack_k_to_n_bitexact(w, K, N):
     want = oracle.pack(oracle.unpack_k(kp))
     assert np.array_equal(got.cpu().numpy(), want)
 
+
+
+@pytest.mark.parametrize("M,K,N,G,dt,asym", [(1, 2112, 1152, 32, "bf16", False), (300, 2048, 768, 64, "f16", True)])
+def test_prepared_layer_equals_the_function(w, M, K, N, G, dt, asym):
+    """W4A16Linear (weights checked once) gives exactly what w4a16_gemm gives, decode and prefill."""
+    c = synth.make_case(M, K, N, G, dt, asym=asym, bias=True, seed=5)
+    t = case_tensors(c)
+    layer = w.W4A16Linear(t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"])
+    got = layer(t["a"])
+    want = w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"])
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    with pytest.raises(ValueError):
+        layer(t["a"][:, :8].contiguous())  # wrong K

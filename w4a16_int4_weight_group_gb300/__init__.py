@@ -246,6 +246,60 @@ def w4a16_gemm(a: torch.Tensor, b_q: torch.Tensor, scales: torch.Tensor, qzeros:
     return out
 
 
+class W4A16Linear:
+    """A prepared W4A16 layer: out[M, N] = a[M, K] @ dequant(W) (+ bias), as w4a16_gemm.
+
+    The weights (b_q, scales, qzeros or zp_bias, bias) are checked once, when the layer is built;
+    each call checks only the activations and the output, so the host work per call is small (decode
+    calls take a few microseconds on the GPU). The layer keeps references to its tensors.
+    """
+
+    def __init__(self, b_q: torch.Tensor, scales: torch.Tensor, qzeros: Optional[torch.Tensor], group_size: int,
+                 zp_bias: int = 8, bias: Optional[torch.Tensor] = None, use_workspace: bool = True):
+        if b_q.dim() != 2 or b_q.dtype != torch.int32:
+            raise ValueError("b_q must be a 2-D int32 tensor [K, N/8]")
+        if qzeros is not None and qzeros.dtype != torch.int32:
+            raise ValueError("qzeros must be int32")
+        if bias is not None and bias.dtype != scales.dtype:
+            raise ValueError("bias must have the dtype of scales")
+        self.device = _require_cuda(b_q, scales, qzeros, bias)
+        self.k, self.n = b_q.shape[0], b_q.shape[1] * 8
+        self.dtype = scales.dtype
+        self.code = _dtype_code(scales.dtype)
+        self.group_size, self.zp_bias = int(group_size), int(zp_bias)
+        self.use_workspace = use_workspace
+        self._tensors = (b_q, scales, qzeros, bias)
+        self._ptrs = (_ptr(b_q), _ptr(scales), _ptr(qzeros))
+        self._bias = _ptr(bias)
+        self._need = {}
+
+    def __call__(self, a: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        if (a.dim() != 2 or a.shape[1] != self.k or a.dtype != self.dtype or a.device != self.device
+                or not a.is_contiguous()):
+            raise ValueError(f"a must be a contiguous [M, {self.k}] {self.dtype} tensor on {self.device}")
+        m = a.shape[0]
+        if out is None:
+            out = torch.empty((m, self.n), dtype=self.dtype, device=self.device)
+        elif (out.shape != (m, self.n) or out.dtype != self.dtype or out.device != self.device
+              or not out.is_contiguous()):
+            raise ValueError(f"out must be a contiguous [{m}, {self.n}] {self.dtype} tensor on {self.device}")
+        stream = _stream(self.device)
+        L = lib()
+        need = 0
+        if self.use_workspace:
+            need = self._need.get(m)
+            if need is None:
+                need = self._need[m] = int(L.w4a16_gemm_workspace_size(m, self.k, self.n, self.group_size, self.code))
+        if need:
+            ws = workspace_for(self.device, stream.value or 0, need)
+            _check(L.w4a16_gemm_ws(_ptr(a), *self._ptrs, self.group_size, self.zp_bias, self._bias, _ptr(out), m,
+                                   self.k, self.n, self.code, _ptr(ws), ws.numel(), stream))
+        else:
+            _check(L.w4a16_gemm(_ptr(a), *self._ptrs, self.group_size, self.zp_bias, self._bias, _ptr(out), m,
+                                self.k, self.n, self.code, stream))
+        return out
+
+
 def w4a16_can_implement(k: int, n: int, group_size: int, dtype, has_g_idx: bool = False):
     """(True, "") or (False, reason), like the pages' can_implement."""
     code = dtype if isinstance(dtype, int) else ({torch.float16: 0, torch.bfloat16: 1}.get(dtype, 99))
