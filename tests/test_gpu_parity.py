@@ -300,3 +300,32 @@ def test_prepared_layer_equals_the_function(w, M, K, N, G, dt, asym):
     assert torch.equal(got.view(torch.int16), want.view(torch.int16))
     with pytest.raises(ValueError):
         layer(t["a"][:, :8].contiguous())  # wrong K
+
+
+def test_plans_of_different_shapes_share_one_workspace(w):
+    """Stream-K calls whose plans differ in grid and tile height, alternating on one workspace
+    buffer: each call's flags must start at zero whatever the previous call left in the partials."""
+    shapes = [(1024, 17408, 5120, 64, "bf16", True), (40, 5120, 7168, 128, "f16", False),
+              (300, 2048, 768, 64, "bf16", False)]
+    cases, plans = [], []
+    for i, (M, K, N, G, dt, asym) in enumerate(shapes):
+        c = synth.make_case(M, K, N, G, dt, asym=asym, bias=True, seed=40 + i)
+        p = w.w4a16_plan(M, K, N, G, 1 if dt == "bf16" else 0, asym, 0, with_workspace=True)
+        assert p["stream_k"] == 1
+        cases.append((c, case_tensors(c)))
+        plans.append((p["grid"], p["m_tile"]))
+    assert len(set(plans)) == len(plans), plans  # all different layouts of the partials
+    need = max(w.w4a16_gemm_workspace_size(c.M, c.K, c.N, c.G, 1 if c.dtype == "bf16" else 0) for c, _ in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    rng = np.random.default_rng(3)
+    for rnd in range(2):
+        for c, t in cases:
+            out = torch.empty((c.M, c.N), dtype=t["a"].dtype, device="cuda")
+            st = w.lib().w4a16_gemm_ws(*[w._ptr(x) for x in (t["a"], t["b_q"], t["scales"], t["qzeros"])], c.G, 8,
+                                       w._ptr(t["bias"]), w._ptr(out), c.M, c.K, c.N,
+                                       1 if c.dtype == "bf16" else 0, w._ptr(ws), need, None)
+            assert st == 0, w.last_error()
+            torch.cuda.synchronize()
+            rows = np.unique(np.linspace(0, c.M - 1, 5).astype(int))
+            check_against_oracle(c, torch_to_bits(out), rows=rows, cols=sample_cols(c.N, rng, k=32),
+                                 label=f"round {rnd} M={c.M}")

@@ -64,8 +64,9 @@ struct PLayout {
   // 32 KB chunks (one epilogue column chunk of all eight warps)
   static constexpr int kFixChunk = 32768;
   static constexpr int kFixSlots = (kOffP - kOffA) / kFixChunk;
-  // + accumulator full/empty, epilogue done, stall test, fix-up ready, fix-up slot full/empty
-  static constexpr int kNumBars = 2 * SA + 2 * SB + 5 + 2 * kFixSlots;
+  // + accumulator full/empty, epilogue done, stall test, fix-up ready, fix-up slot full/empty,
+  // accumulators released (teardown)
+  static constexpr int kNumBars = 2 * SA + 2 * SB + 6 + 2 * kFixSlots;
   static constexpr int kOffSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffFlag = kOffSlot + 4;
   static constexpr int kSmemUsed = kOffFlag + 4;
@@ -234,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kFixSlots = L::kFixSlots;
   auto fix_full = [&](int s) { return fix_ready + 8u * (1 + s); };
   auto fix_empty = [&](int s) { return fix_ready + 8u * (1 + kFixSlots + s); };
+  const uint32_t tmem_done = fix_ready + 8u * (1 + 2 * kFixSlots);  // every epilogue warp is past TMEM
   const uint32_t abort_flag = base + kOffFlag;
   const uint32_t slot = base + kOffSlot;
 
@@ -258,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(fix_full(s), 1);
       mbar_init(fix_empty(s), kDequantWarps);
     }
+    mbar_init(tmem_done, kDequantWarps);
     st_flag(abort_flag, 0u);
     mbar_init_fence();
   }
@@ -489,19 +492,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // without its end is always this CTA's last segment: the producer thread stages the
         // contributors' partial tiles (fix-up loader) once all MMAs are done.
         const int64_t c_last = (owner && !whole) ? c_fix : int64_t(blockIdx.x);
-#pragma unroll 1
-        for (int it = 0; it < 4 * MT; ++it) {
+        // One 32-column chunk of the accumulators (it: accumulator mt = it / 4, chunk it % 4), already
+        // loaded from TMEM into r.
+        auto epi_chunk = [&](uint32_t (&r)[32], int it) {
           const int mt = it >> 2, ch = it & 3;  // accumulator (row half of the tile) and 32-column chunk
           const int tr = 128 * mt + row;        // row within the tile
           const int64_t m = m0 + tr;
           const bool row_ok = m < p.M;
           const int col0 = half * 128 + ch * 32;
-          uint32_t r[32];
-          if (ok) {
-            tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(256 * mt + col0), r);
-            tmem_wait_ld();
-          }
-          if (!ok) continue;
           // partial tiles travel in accumulator order: chunk `it` of a CTA is 32 KB, float4 j of
           // thread (dw, lane) at ((dw * 8 + j) * 32 + lane) * 16 bytes (a warp's float4 j is 512
           // contiguous bytes)
@@ -514,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 8; ++j)
               dst[32 * j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                         __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-            continue;
+            return;
           }
           if (!whole) {
             // add the contributors' chunks in CTA order (deterministic), as the loader stages them
@@ -537,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(fix_empty(sl));
             }
-            if (!ok) continue;
+            if (!ok) return;
           }
           // Two 8-column groups at a time: 16 outputs = 32 bytes per store (a whole sector of the
           // row) when the rows and the output pointer are 32-byte aligned; 16-byte stores otherwise.
@@ -588,6 +586,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (n + 8 < p.N) *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(o[4], o[5], o[6], o[7]);
             }
           }
+        };
+        auto tmem_chunk = [&](int it) {
+          return tmem + (uint32_t(32 * q) << 16) + uint32_t(256 * (it >> 2) + half * 128 + (it & 3) * 32);
+        };
+        // TMEM loads double-buffered: chunk it + 1 is in flight while chunk it is processed
+        uint32_t ra[32], rb[32];
+        if (ok) {
+          tmem_ld32(tmem_chunk(0), ra);
+          tmem_wait_ld();
+        }
+#pragma unroll 1
+        for (int it = 0; it < 4 * MT && ok; it += 2) {
+          tmem_ld32(tmem_chunk(it + 1), rb);
+          epi_chunk(ra, it);
+          tmem_wait_ld();
+          if (!ok) break;
+          if (it + 2 < 4 * MT) tmem_ld32(tmem_chunk(it + 2), ra);
+          epi_chunk(rb, it + 1);
+          tmem_wait_ld();
         }
         // the accumulators have been read: the next segment's MMAs may overwrite them
         tc_fence_before();
@@ -619,15 +636,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++t;
       }
     }
+    // this warp's TMEM reads are complete (each tcgen05.ld was waited on): release the accumulators
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tmem_done);
   }
 
-  // Warps 0 and 1 ran their roles on lane 0 only: reconverge each warp before the block-wide barrier,
-  // so that no lane reaches it ahead of its warp (the barrier counts warps) and TMEM is released only
-  // after every epilogue warp has read its accumulators.
+  // Teardown. Warps 0 and 1 ran their roles on lane 0 only: reconverge them first. TMEM is freed
+  // only once every epilogue warp has signalled (mbarrier) that its last tcgen05.ld is complete:
+  // measured, the block barrier alone let warp 1 through while epilogue warps were still reading.
   __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    drain_phase(tmem_done, 0, &g_prefill_error);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
