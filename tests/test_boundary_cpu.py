@@ -136,11 +136,13 @@ def test_prefill_plan_stream_k_with_a_workspace(w):
     # few tiles: fewer CTAs than SMs, so that the owner's fix-up stays short
     p = w.w4a16_plan(256, 4096, 1024, 32, 1, True, 152)
     assert p["stream_k"] == 1 and 4 < p["grid"] < 152, p
-    # mid M (17..128): 128-row tiles would leave most SMs idle; stream-K over 128-row tiles fills them
+    # mid M (17..128): one CTA per 128-row tile would leave most SMs idle; clusters of CTAs split each
+    # tile's K blocks and add their partial tiles through distributed shared memory (no workspace)
     for m in (17, 32, 64, 128):
-        p = w.w4a16_plan(m, 5120, 7168, 128, 1, False, 152)
-        assert p["path_name"] == "prefill" and p["stream_k"] == 1 and p["m_tile"] == 128, (m, p)
-        assert p["grid"] >= 100, (m, p)
+        for ws in (True, False):
+            p = w.w4a16_plan(m, 5120, 7168, 128, 1, False, 152, with_workspace=ws)
+            assert p["path_name"] == "prefill" and p["m_tile"] == 128 and p["stream_k"] == 0, (m, p)
+            assert 2 <= p["k_split"] <= 8 and p["grid"] == 28 * p["k_split"] and p["grid"] >= 100, (m, p)
 
 
 def test_dispatcher_uses_runtime_m_not_a_frozen_config(w):

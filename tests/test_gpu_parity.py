@@ -223,7 +223,7 @@ def test_sweep_shapes_sampled(w, M, K, N, G):
 
 @pytest.mark.parametrize("M,K,N,G,dt,asym", [(512, 4096, 1024, 128, "bf16", True), (300, 2048, 768, 64, "f16", False),
                                            (1024, 17408, 5120, 64, "bf16", True), (256, 4096, 1024, 32, "bf16", True),
-                                           (40, 5120, 7168, 128, "f16", True)])
+                                           (192, 5120, 7168, 128, "f16", True)])
 def test_stream_k_matches_oracle_and_leaves_workspace_clean(w, M, K, N, G, dt, asym):
     """Persistent stream-K prefill: several CTAs share each output tile through the workspace; the
     tile's owner stages their partial tiles in rounds through its shared memory (more chunks than
@@ -305,7 +305,7 @@ def test_prepared_layer_equals_the_function(w, M, K, N, G, dt, asym):
 def test_plans_of_different_shapes_share_one_workspace(w):
     """Stream-K calls whose plans differ in grid and tile height, alternating on one workspace
     buffer: each call's flags must start at zero whatever the previous call left in the partials."""
-    shapes = [(1024, 17408, 5120, 64, "bf16", True), (40, 5120, 7168, 128, "f16", False),
+    shapes = [(1024, 17408, 5120, 64, "bf16", True), (192, 5120, 7168, 128, "f16", False),
               (300, 2048, 768, 64, "bf16", False)]
     cases, plans = [], []
     for i, (M, K, N, G, dt, asym) in enumerate(shapes):
@@ -329,3 +329,26 @@ def test_plans_of_different_shapes_share_one_workspace(w):
             rows = np.unique(np.linspace(0, c.M - 1, 5).astype(int))
             check_against_oracle(c, torch_to_bits(out), rows=rows, cols=sample_cols(c.N, rng, k=32),
                                  label=f"round {rnd} M={c.M}")
+
+
+@pytest.mark.parametrize("M,K,N,G,dt,asym", [(40, 5120, 7168, 128, "f16", True), (100, 2112, 1152, 32, "bf16", False),
+                                           (128, 17408, 5120, 17408, "bf16", True)])
+def test_cluster_split_k_mid_m(w, M, K, N, G, dt, asym):
+    """Mid M: the CTAs of a cluster split each 128-row tile's K blocks and add their partial tiles
+    through distributed shared memory in rank order: oracle parity, determinism, no workspace."""
+    c = synth.make_case(M, K, N, G, dt, asym=asym, bias=True, seed=M + 3)
+    code = 1 if dt == "bf16" else 0
+    plan = w.w4a16_plan(M, K, N, G, code, asym, 0, with_workspace=False)
+    assert plan["path_name"] == "prefill" and plan["k_split"] > 1 and plan["stream_k"] == 0, plan
+    t = case_tensors(c)
+    outs = []
+    for _ in range(2):
+        out = w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"], use_workspace=False)
+        torch.cuda.synchronize()
+        outs.append(torch_to_bits(out))
+    assert np.array_equal(outs[0], outs[1]), "cluster split-K must be deterministic"
+    assert w.w4a16_get_device_error() == 0
+    rng = np.random.default_rng(M)
+    rows = sorted({0, M - 1} | set(rng.integers(0, M, size=6).tolist()))
+    check_against_oracle(c, outs[0], rows=rows, cols=sample_cols(N, rng, k=128), label="cluster split-K")
+

@@ -116,7 +116,7 @@ void choose_plan(const GemmArgs &g, int num_sms, bool tma, bool query_device, bo
   if (path == W4A16_PATH_DECODE) {
     decode_make_plan(g.M, g.K, g.N, g.group_size, num_sms, query_device, p);
   } else if (path == W4A16_PATH_PREFILL) {
-    prefill_make_plan(g.M, g.K, g.N, g.group_size, num_sms, workspace, p);
+    prefill_make_plan(g.M, g.K, g.N, g.group_size, num_sms, workspace, query_device, p);
   } else {
     p->path = W4A16_PATH_GENERIC;
     p->m_tile = 8;

@@ -165,6 +165,12 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
   return r;
 }
+// 16-byte load from another CTA's shared memory (a shared::cluster address, 16-byte aligned).
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr) {
+  float4 v;
+  asm("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(cluster_addr));
+  return v;
+}
 // Plain (non-volatile) load so that the compiler may issue several remote loads back to back; the
 // ordering against the writers comes from the cluster barrier that precedes the reads.
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {

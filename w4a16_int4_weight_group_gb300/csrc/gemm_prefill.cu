@@ -149,6 +149,7 @@ struct PrefillParams {
   int64_t tiles;     // m_tiles x column tiles
   float *partials;   // stream-K: one fp32 [BM][BN] partial tile per CTA (null when every CTA owns whole tiles)
   unsigned int *flags;  // stream-K: per-CTA "partial ready" flags; zero before and after every launch
+  int csplit;        // > 1: clusters of csplit CTAs split each tile's K blocks (128-row tiles only)
 };
 
 // First (tile, K block) work unit of CTA c when the tiles x nk units are split evenly over G CTAs.
@@ -208,15 +209,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nk = p.nk;
   const int64_t total = p.tiles * nk;
   const int64_t G = gridDim.x;
-  const int64_t u_begin = unit_begin(blockIdx.x, total, G);
-  const int64_t u_end = unit_begin(int64_t(blockIdx.x) + 1, total, G);
+  // Cluster split-K: the C CTAs of a cluster share one tile, rank r taking K blocks
+  // [r nk / C, (r + 1) nk / C); their partial tiles meet in distributed shared memory.
+  const int C = p.csplit;
+  const int64_t u_begin = C > 1 ? (blockIdx.x / C) * int64_t(nk) + int64_t(blockIdx.x % C) * nk / C
+                                : unit_begin(blockIdx.x, total, G);
+  const int64_t u_end = C > 1 ? (blockIdx.x / C) * int64_t(nk) + int64_t(blockIdx.x % C + 1) * nk / C
+                              : unit_begin(int64_t(blockIdx.x) + 1, total, G);
   const int n_units = static_cast<int>(u_end - u_begin);
   const int64_t t_first = u_begin / nk;
   const int kb_first = static_cast<int>(u_begin - t_first * nk);
   // The share's last segment needs a fix-up when it starts a tile (K block 0) but ends inside it: the
   // CTAs after this one hold the rest of that tile and publish their partial tiles.
   const int64_t t_last = n_units > 0 ? (u_end - 1) / nk : t_first;
-  const bool fix_needed = n_units > 0 && (t_last > t_first || kb_first == 0) && u_end < (t_last + 1) * nk;
+  const bool fix_needed = C == 1 && n_units > 0 && (t_last > t_first || kb_first == 0) && u_end < (t_last + 1) * nk;
   int64_t c_fix = blockIdx.x;  // last CTA holding part of tile t_last
   if (fix_needed)
     while (c_fix + 1 < G && unit_begin(c_fix + 1, total, G) < (t_last + 1) * nk) ++c_fix;
@@ -504,6 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // thread (dw, lane) at ((dw * 8 + j) * 32 + lane) * 16 bytes (a warp's float4 j is 512
           // contiguous bytes)
           const uint32_t lane_off = uint32_t((dw * 8 * 32 + lane) * 16);
+          if (C > 1) {
+            // cluster split-K: stage this CTA's partial tile in its own (now idle) stage buffers
+            const uint32_t dst = base + kOffA + it * L::kFixChunk + lane_off;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sts128(dst + 512u * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            return;
+          }
           if (!owner) {
             // publish this CTA's partial tile
             float4 *dst = reinterpret_cast<float4 *>(p.partials + (int64_t(blockIdx.x) * (4 * MT) + it) * (L::kFixChunk / 4)) +
@@ -612,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(accum_empty);
         // partial tiles: publish (contributor) or release the consumed flags (owner), once every
         // epilogue warp is done with its stores / reads (a bounded mbarrier wait, not a hard barrier)
-        if (!whole) {
+        if (!whole && C == 1) {
           __threadfence();
           __syncwarp();
           if (lane == 0) mbar_arrive(epi_done);
@@ -640,6 +653,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(tmem_done);
+  }
+
+  if (C > 1) {
+    // Cluster split-K reduction. Every thread of every rank arrives (the roles above end without
+    // early exits), so both cluster barriers complete. After the first, all ranks' staged partial
+    // tiles are visible; rank r then adds its share of the tile's 8-column groups over all ranks in
+    // rank order (deterministic) and stores them; the second keeps the staging alive until every
+    // rank has read it.
+    __syncwarp();
+    cluster_sync_all();
+    const int64_t t = blockIdx.x / C;
+    const int r = static_cast<int>(blockIdx.x % C);
+    const int64_t m0 = (t % p.m_tiles) * BM, n0 = (t / p.m_tiles) * BN;
+    constexpr int kUnits = 4 * MT * kDequantWarps * 4 * 32;  // chunks x warps x 8-column groups x lanes
+    const int u0 = r * kUnits / C, u1 = (r + 1) * kUnits / C;
+    for (int u = u0 + static_cast<int>(threadIdx.x); u < u1; u += kThreads) {
+      const int ln = u & 31, g8 = (u >> 5) & 3, dwv = (u >> 7) & 7, it = u >> 10;
+      const int qv = (dwv + 2) & 3, hv = dwv >> 2, mt = it >> 2, ch = it & 3;
+      const int64_t m = m0 + 128 * mt + 32 * qv + ln;
+      const int64_t n = n0 + hv * 128 + ch * 32 + 8 * g8;
+      // the group's raw accumulator order sits in float4 j = 2 g8 and 2 g8 + 1 of thread (dwv, ln)
+      const uint32_t off = base + kOffA + it * L::kFixChunk + uint32_t(((dwv * 8 + 2 * g8) * 32 + ln) * 16);
+      float4 xa[8], xb[8];
+#pragma unroll
+      for (int src = 0; src < 8; ++src) {
+        if (src < C) {
+          const uint32_t a = map_to_rank(off, static_cast<uint32_t>(src));
+          xa[src] = ld_dsmem_v4(a);
+          xb[src] = ld_dsmem_v4(a + 512u);
+        }
+      }
+      float raw[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int src = 0; src < 8; ++src) {
+        if (src < C) {
+          raw[0] += xa[src].x; raw[1] += xa[src].y; raw[2] += xa[src].z; raw[3] += xa[src].w;
+          raw[4] += xb[src].x; raw[5] += xb[src].y; raw[6] += xb[src].z; raw[7] += xb[src].w;
+        }
+      }
+      if (m >= p.M || n >= p.N) continue;
+      // raw columns hold outputs n+0, n+4, n+1, n+5, n+2, n+6, n+3, n+7
+      float v[8] = {raw[0], raw[2], raw[4], raw[6], raw[1], raw[3], raw[5], raw[7]};
+      if (p.bias) {
+        const uint4 bv = *reinterpret_cast<const uint4 *>(p.bias + n);
+        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[2 * e] += bits_to_float(static_cast<uint16_t>(bw[e] & 0xFFFFu), BF);
+          v[2 * e + 1] += bits_to_float(static_cast<uint16_t>(bw[e] >> 16), BF);
+        }
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (BF) {
+          const __nv_bfloat162 tt = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+          o[e] = *reinterpret_cast<const uint32_t *>(&tt);
+        } else {
+          const __half2 tt = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
+          o[e] = *reinterpret_cast<const uint32_t *>(&tt);
+        }
+      }
+      *reinterpret_cast<uint4 *>(p.out + m * p.N + n) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    cluster_sync_relaxed();
   }
 
   // Teardown. Warps 0 and 1 ran their roles on lane 0 only: reconverge them first. TMEM is freed
@@ -692,18 +770,54 @@ size_t prefill_plan_workspace_bytes(const w4a16_plan_t &pl) {
 
 size_t prefill_workspace_bytes(int64_t M, int64_t K, int64_t N, int group_size, int num_sms) {
   w4a16_plan_t pl;
-  prefill_make_plan(M, K, N, group_size, num_sms, /*workspace=*/true, &pl);
+  prefill_make_plan(M, K, N, group_size, num_sms, /*workspace=*/true, /*query_device=*/false, &pl);
   return prefill_plan_workspace_bytes(pl);
 }
 
+// CTAs of the 128-row-tile kernel resident at once when launched in clusters of C: queried from the
+// runtime (clusters live within a GPC), once per device and C; 0 when unknown.
+static int64_t cluster_slots(int C) {
+  static std::mutex mu;
+  static int cache[64][9];
+  static bool have[64][9] = {};
+  int dev = 0;
+  if (C < 2 || C > 8 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[dev][C]) {
+    const KernelFn fn = pick(W4A16_F16, false, false, 1);
+    int n = 0;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_of(1)) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(C), 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = static_cast<size_t>(smem_of(1));
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = static_cast<unsigned>(C);
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess) n = clusters * C;
+    }
+    cudaGetLastError();  // a failed query leaves no sticky state
+    cache[dev][C] = n;
+    have[dev][C] = true;
+  }
+  return cache[dev][C];
+}
+
 void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool workspace,
-                       w4a16_plan_t *p) {
+                       bool query_device, w4a16_plan_t *p) {
   (void)group_size;
   // Cost in units of one (256-row tile, K block) step of the two-accumulator kernel. One CTA per SM.
   //  * one CTA per tile: waves x K blocks; a 128-row step costs 0.7 (dequantisation is not halved);
   //  * stream-K over G CTAs (needs the workspace): an even share of all steps per CTA, plus the
-  //    owner's fix-up, ~2 steps per contributor whose partial tile it adds (a 256 KB read; half that
-  //    for 128-row tiles).
+  //    owner's fix-up, ~3 steps per contributor whose partial tile it waits for and adds (measured);
+  //  * 128-row tiles split along K over clusters of C <= 8 CTAs, partial tiles added through
+  //    distributed shared memory (no workspace): waves x (K blocks / C steps + ~2 for the exchange),
+  //    with the co-resident cluster count from the runtime (clusters fit within a GPC).
   const int64_t n_tiles = (N + BN - 1) / BN;
   const int64_t nk = (K + BK - 1) / BK;
   const int64_t sms = std::max(1, num_sms);
@@ -711,6 +825,7 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
   int MT = 2;
   int64_t grid = 0;
   bool stream_k = false;
+  int csplit = 1;
   for (int mt = 2; mt >= 1; --mt) {
     const int64_t tiles = ((M + 128 * mt - 1) / (128 * mt)) * n_tiles;
     const double cost = double((tiles + sms - 1) / sms) * double(nk) * (mt == 1 ? 0.7 : 1.0);
@@ -727,7 +842,7 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
     for (int mt = 2; mt >= 1; --mt) {
       const int64_t tiles = ((M + 128 * mt - 1) / (128 * mt)) * n_tiles;
       const int64_t total = tiles * nk;
-      const double step = mt == 1 ? 0.7 : 1.0, fix = mt == 1 ? 1.0 : 2.0;
+      const double step = mt == 1 ? 0.7 : 1.0, fix = 3.0;
       for (int64_t g = 1; g <= std::min<int64_t>(std::min<int64_t>(sms, kMaxStreamKCtas), total); ++g) {
         const int64_t share = (total + g - 1) / g;
         const int64_t parts = (g + tiles - 1) / tiles + 1;  // CTAs touching one tile, at most
@@ -741,11 +856,29 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
       }
     }
   }
+  if (M <= 128 && nk >= 2) {
+    const int64_t tiles = n_tiles;  // one 128-row tile per column tile
+    for (int c = 2; c <= 8 && c <= nk; ++c) {
+      int64_t slots = query_device ? cluster_slots(c) : 0;
+      // without a device: GPCs of 19 SMs (GB300: 8 x 19), whole clusters per GPC
+      if (slots <= 0) slots = std::max<int64_t>(1, sms / 19) * (19 / c) * c;
+      if (slots <= 0) continue;
+      const int64_t waves = (tiles * c + slots - 1) / slots;
+      const double cost = double(waves) * (double((nk + c - 1) / c) * 0.7 + 2.0);
+      if (cost < best - 1e-9) {
+        best = cost;
+        MT = 1;
+        grid = tiles * c;
+        stream_k = false;
+        csplit = c;
+      }
+    }
+  }
   p->path = W4A16_PATH_PREFILL;
   p->k_blocks_per_stage = 1;
   p->m_tile = 128 * MT;
   p->n_tile = BN;
-  p->k_split = 1;
+  p->k_split = csplit;  // > 1: clusters of k_split CTAs per 128-row tile
   p->warps = kThreads / 32;
   p->grid = grid;
   p->smem_bytes = smem_of(MT);
@@ -805,17 +938,29 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl) {
   prm.G = g.group_size;
   prm.zp_bias = g.zp_bias;
   prm.nk = static_cast<int>((g.K + BK - 1) / BK);
+  prm.csplit = pl.k_split > 1 ? pl.k_split : 1;
+  if (prm.csplit > 1 && (MT != 1 || pl.stream_k || pl.grid % prm.csplit != 0 || prm.nk < prm.csplit))
+    return cudaErrorInvalidValue;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_of(MT);
   cfg.stream = g.stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
+  cudaLaunchAttribute attr[2];
+  int nattr = 0;
+  attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+  ++nattr;
+  if (prm.csplit > 1) {
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = static_cast<unsigned>(prm.csplit);
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = nattr;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tA, tP, tS, tZ, prm);
   if (e != cudaSuccess) return e;
   note_launch();

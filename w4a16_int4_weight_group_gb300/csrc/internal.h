@@ -68,7 +68,7 @@ cudaError_t decode_set_stall(bool on);
 bool prefill_supported(const GemmArgs &g);
 // workspace: a scratch buffer will be available (stream-K may be chosen).
 void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool workspace,
-                       w4a16_plan_t *p);
+                       bool query_device, w4a16_plan_t *p);
 size_t prefill_workspace_bytes(int64_t M, int64_t K, int64_t N, int group_size, int num_sms);
 // Workspace bytes a prefill plan needs (0 unless it is stream-K).
 size_t prefill_plan_workspace_bytes(const w4a16_plan_t &plan);
