@@ -6,7 +6,11 @@
 // snippets: fp32 accumulator, dequantise then multiply-add per K tile). On sm_103a this becomes:
 //
 //  * CTA tile 128*MT (rows of A; MT = 1 or 2 accumulators) x 256 (output columns), K in blocks of
-//    64. One CTA per tile, 10 warps:
+//    64. Work is a list of (tile, K block) units, split three ways (the host plan picks by a cost
+//    model): one CTA per tile; persistent stream-K, each CTA an equal contiguous share of the units,
+//    partial tiles meeting through the caller's workspace; or, for 128-row problems, the C CTAs of a
+//    thread-block cluster splitting one tile's K blocks, partial tiles meeting in distributed shared
+//    memory. 10 warps per CTA:
 //      warp 0      TMA producer: A tile (128x64, 128-byte swizzle), packed weight tile (64 rows x 32
 //                  words), the one or two scale rows and zero-point rows the block needs;
 //      warp 1      TMEM allocator and the single MMA-issuing thread;
@@ -26,8 +30,11 @@
 //    full/empty mbarriers. Every wait is bounded (default 2 s, settable for tests): on expiry the CTA
 //    records an error word, stops, drains its own TMA copies and MMAs with a fixed bound, frees its
 //    TMEM and exits without writing output.
-//  * Epilogue: tcgen05.ld 32 columns at a time, + bias in fp32, one rounding to the dtype, 16-byte
-//    stores (PR #40977 report, key source snippets, test reference: bias before the cast).
+//  * Epilogue: tcgen05.ld 32 columns at a time (double-buffered), + bias in fp32, one rounding to
+//    the dtype, 32-byte stores when aligned (PR #40977 report, key source snippets, test reference:
+//    bias before the cast). Split tiles: contributors publish fp32 partials (stream-K: workspace;
+//    cluster: own shared memory); the tile owner (stream-K) or every rank (cluster, a share each)
+//    adds them in CTA order, so results do not depend on timing.
 #include <algorithm>
 #include <mutex>
 
