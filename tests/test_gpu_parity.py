@@ -332,7 +332,7 @@ def test_plans_of_different_shapes_share_one_workspace(w):
 
 
 @pytest.mark.parametrize("M,K,N,G,dt,asym", [(40, 5120, 7168, 128, "f16", True), (100, 2112, 1152, 32, "bf16", False),
-                                           (128, 17408, 5120, 17408, "bf16", True)])
+                                           (128, 17408, 5120, 17408, "bf16", True), (17, 1152, 2112, 32, "bf16", False)])
 def test_cluster_split_k_mid_m(w, M, K, N, G, dt, asym):
     """Mid M: the CTAs of a cluster split each 128-row tile's K blocks and add their partial tiles
     through distributed shared memory in rank order: oracle parity, determinism, no workspace."""

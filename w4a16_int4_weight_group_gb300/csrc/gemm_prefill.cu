@@ -157,6 +157,7 @@ struct PrefillParams {
   float *partials;   // stream-K: one fp32 [BM][BN] partial tile per CTA (null when every CTA owns whole tiles)
   unsigned int *flags;  // stream-K: per-CTA "partial ready" flags; zero before and after every launch
   int csplit;        // > 1: clusters of csplit CTAs split each tile's K blocks (128-row tiles only)
+  int a_rows;        // rows of A per TMA box: BM, or M rounded up to 8 when one row tile covers M
 };
 
 // First (tile, K block) work unit of CTA c when the tiles x nk units are split evenly over G CTAs.
@@ -299,7 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint32_t tx = kABytes + kPBytes + srows * (BN * 2) + (HAS_ZP ? srows * (BN / 8) * 4 : 0);
+      // With a single row tile only the rows up to M (rounded up to 8) are fetched; the MMA still reads
+      // BM rows of the stage, and the stale rows past them only reach accumulator rows past M, which
+      // nothing stores (row m of the product depends on row m of A alone).
+      const uint32_t tx = uint32_t(p.a_rows) * (BK * 2) + kPBytes + srows * (BN * 2) + (HAS_ZP ? srows * (BN / 8) * 4 : 0);
       int issued = 0;
       int64_t t = t_first;
       int kb = kb_first;
@@ -610,14 +614,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto tmem_chunk = [&](int it) {
           return tmem + (uint32_t(32 * q) << 16) + uint32_t(256 * (it >> 2) + half * 128 + (it & 3) * 32);
         };
+        // A warp whose accumulator rows all lie past M has nothing to store; it skips its chunks
+        // unless the stream-K exchange counts on it (contributor publishing, owner adding).
+        const bool live = (C == 1 && !whole) || m0 + 32 * q < p.M;
         // TMEM loads double-buffered: chunk it + 1 is in flight while chunk it is processed
         uint32_t ra[32], rb[32];
-        if (ok) {
+        if (ok && live) {
           tmem_ld32(tmem_chunk(0), ra);
           tmem_wait_ld();
         }
 #pragma unroll 1
-        for (int it = 0; it < 4 * MT && ok; it += 2) {
+        for (int it = 0; it < 4 * MT && ok && live; it += 2) {
           tmem_ld32(tmem_chunk(it + 1), rb);
           epi_chunk(ra, it);
           tmem_wait_ld();
@@ -673,13 +680,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t t = blockIdx.x / C;
     const int r = static_cast<int>(blockIdx.x % C);
     const int64_t m0 = (t % p.m_tiles) * BM, n0 = (t / p.m_tiles) * BN;
-    constexpr int kUnits = 4 * MT * kDequantWarps * 4 * 32;  // chunks x warps x 8-column groups x lanes
-    const int u0 = r * kUnits / C, u1 = (r + 1) * kUnits / C;
+    // units: (row, 8-column group) pairs of the rows below M, rows fastest (a warp reads contiguous
+    // staged float4s); rank r takes an even share
+    const int nrows = static_cast<int>(p.M - m0 < BM ? p.M - m0 : BM);
+    const int n_units_red = nrows * (BN / 8);
+    const int u0 = r * n_units_red / C, u1 = (r + 1) * n_units_red / C;
     for (int u = u0 + static_cast<int>(threadIdx.x); u < u1; u += kThreads) {
-      const int ln = u & 31, g8 = (u >> 5) & 3, dwv = (u >> 7) & 7, it = u >> 10;
-      const int qv = (dwv + 2) & 3, hv = dwv >> 2, mt = it >> 2, ch = it & 3;
-      const int64_t m = m0 + 128 * mt + 32 * qv + ln;
-      const int64_t n = n0 + hv * 128 + ch * 32 + 8 * g8;
+      const int tr = u % nrows, cg = u / nrows;
+      const int mt = tr >> 7, qv = (tr >> 5) & 3, ln = tr & 31;
+      const int hv = cg >> 4, ch = (cg >> 2) & 3, g8 = cg & 3;
+      // the staging warp of these rows and columns: (dw + 2) % 4 = quarter, dw / 4 = column half
+      const int dwv = 4 * hv + ((qv + 2) & 3), it = 4 * mt + ch;
+      const int64_t m = m0 + tr;
+      const int64_t n = n0 + 8 * cg;
+      if (n >= p.N) continue;
       // the group's raw accumulator order sits in float4 j = 2 g8 and 2 g8 + 1 of thread (dwv, ln)
       const uint32_t off = base + kOffA + it * L::kFixChunk + uint32_t(((dwv * 8 + 2 * g8) * 32 + ln) * 16);
       float4 xa[8], xb[8];
@@ -699,7 +713,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           raw[4] += xb[src].x; raw[5] += xb[src].y; raw[6] += xb[src].z; raw[7] += xb[src].w;
         }
       }
-      if (m >= p.M || n >= p.N) continue;
       // raw columns hold outputs n+0, n+4, n+1, n+5, n+2, n+6, n+3, n+7
       float v[8] = {raw[0], raw[2], raw[4], raw[6], raw[1], raw[3], raw[5], raw[7]};
       if (p.bias) {
@@ -899,8 +912,10 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl) {
   const int64_t NW = g.N / 8, ng = g.K / g.group_size;
   const bool two = g.group_size < BK && g.group_size != g.K;  // G = 32: two groups per K block
   const int srows = two ? 2 : 1;
+  // one row tile: fetch only the rows up to M (rounded up to 8) of each A block
+  const int a_rows = g.M <= BM ? static_cast<int>((g.M + 7) / 8 * 8) : BM;
   CUtensorMap tA, tP, tS, tZ;
-  if (!tma_encode_2d(&tA, 2, g.a, g.K, g.M, g.K * 2, BK, BM, true) ||
+  if (!tma_encode_2d(&tA, 2, g.a, g.K, g.M, g.K * 2, BK, a_rows, true) ||
       !tma_encode_2d(&tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK, false) ||
       !tma_encode_2d(&tS, 2, g.scales, g.N, ng, g.N * 2, BN, srows, false))
     return cudaErrorInvalidValue;
@@ -946,6 +961,7 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl) {
   prm.zp_bias = g.zp_bias;
   prm.nk = static_cast<int>((g.K + BK - 1) / BK);
   prm.csplit = pl.k_split > 1 ? pl.k_split : 1;
+  prm.a_rows = a_rows;
   if (prm.csplit > 1 && (MT != 1 || pl.stream_k || pl.grid % prm.csplit != 0 || prm.nk < prm.csplit))
     return cudaErrorInvalidValue;
 
