@@ -21,17 +21,17 @@
 //    ldmatrix.trans delivers to lane (g, t) the element of rows 2t and 2t+1 for column quad g: the
 //    two rows of a k pair side by side, which is what a 16-bit MMA register holds. The 128-byte
 //    swizzle makes the eight row addresses of each 8x8 matrix hit distinct banks.
-//  * Dequantisation folded into the product. One LOP3 places the nibble of column j of both rows
+//  * Dequantisation split around the product. One LOP3 places the nibble of column j of both rows
 //    of a k pair into the low mantissa bits of a packed fp16 pair with exponent of 1024 (64 for the
-//    high nibble of a byte) or a bf16 pair with exponent of 128: exactly (base+q_k, base+q_k+1).
-//    The tensor core multiplies these exact integers by the activations (blk), and the same
-//    activation fragments by ones (sa = row sums of A over the group's k steps). Per K block and
-//    group, in fp32: acc += s * (blk - (base + zp) * sa), which equals s * sum_k A (q - zp) up to fp32
-//    rounding. The scale is applied in fp32, so the weights are never rounded to 16 bits; with
-//    one-hot activations the result is exactly RNE(s * (q - zp)), the value w4a16_dequant writes.
+//    high nibble of a byte) or a bf16 pair with exponent of 128: exactly (base+q_k, base+q_k+1). One
+//    packed subtraction of (base + zp) leaves q - zp, a small integer and so exact in 16 bits. The
+//    tensor core multiplies these by the activations (blk = sum_k A (q - zp) in fp32); per K block
+//    and group, in fp32: acc += s * blk. The scale is applied in fp32, so the weights are never
+//    rounded to 16 bits; with one-hot activations the result is exactly RNE(s * (q - zp)), the value
+//    w4a16_dequant writes.
 //  * Multiply. mma.sync m16n8k16 with 16 output columns as the MMA rows and up to 8 rows of A as the
 //    MMA columns (the M <= 8 decode batch fills the n=8 side; M <= 16 takes two MMAs). Per warp and
-//    K block: 8 LOP3-based unpacks of 8 weights each, 12 MMAs (8 products, 4 row sums) and 16 FFMAs.
+//    K block: 8 LOP3-based unpacks of 8 weights each, 32 packed subtractions, 8 MMAs and 8 FFMAs.
 //  * Epilogue. Bias is added in fp32 and the sum rounded once to the activation dtype (PR #40977
 //    report, key source snippets, test reference).
 //  * Every mbarrier wait is bounded: on expiry the CTA records an error word, its warps leave the
@@ -98,13 +98,6 @@ struct DecodeParams {
   int g_shift;      // log2(G) when a stage spans several scale groups, else 31 (one group per stage)
 };
 
-// Magic base of column j of a quad (see magic_quad): fp16 uses 1024 for the low nibble of a byte
-// (even j) and 64 for the high nibble (odd j, mantissa ulp 1/16); bf16 uses 128.
-template <bool BF>
-__device__ __forceinline__ float magic_base(int j) {
-  if constexpr (BF) return 128.f;
-  else return (j & 1) ? 64.f : 1024.f;
-}
 // A 16-bit float (fp16 or bf16 bits) widened exactly to fp32.
 template <bool BF>
 __device__ __forceinline__ float bits_to_f32(uint32_t h) {
@@ -268,14 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Column j of this lane's quad (output column n0 + 32 cb + 4 gl + j) holds magic values base_j + q:
     // fp16 uses 1024 for even j (low nibble of a byte) and 64 for odd j (high nibble), bf16 uses 128.
-    // zc[j] = base_j + zp and sc[j] = scale, both fp32, for the group being processed.
-    float zc[4], sc[4];
-    if constexpr (!HAS_ZP) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) zc[j] = magic_base<BF>(j) + static_cast<float>(p.zp_bias);
-    }
-    const uint32_t one2 = BF ? 0x3F803F80u : 0x3C003C00u;  // (1, 1) in the activation dtype
-    const uint32_t ones[4] = {one2, one2, one2, one2};
+    // zsub[j] = (base_j + zp, base_j + zp) in the activation dtype: the same unpack applied to a word
+    // whose four nibbles are the zero points, in both halves. sc[j] = scale (fp32).
+    uint32_t zsym[4];
+    float sc[4];
+    if constexpr (!HAS_ZP) magic_quad<BF>(static_cast<uint32_t>(p.zp_bias) * 0x11111111u, zsym);
     bool ok = true;
     if (g_decode_stall) {  // failure-detection test: a wait that can only run out
       ok = wait_phase(stall_bar, 0, abort_flag, limit_ns, &g_decode_error);
@@ -324,17 +314,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && (((i + kGroups) >> sbs) != js || i + kGroups >= nkb)) mbar_arrive(empty0 + 8u * s);
       return true;
     };
-    // Exact products on the tensor core for scale group g of a block: blk = sum_k A[m,k] (base_j +
-    // q[k,n]) over the group's k16 steps, and sa = sum_k A[m,k] from the same activation fragments
-    // against ones. Then (blk - (base_j + zp) sa) = sum_k A (q - zp), and one fp32 multiply by the scale.
-    auto products = [&](const Frag &f, int g, float (&blk)[J][2][4], float (&sa)[J][4]) {
+    // Products on the tensor core for scale group g of a block: one packed subtraction per pair turns
+    // (base_j + q) into q - zp, exactly (a small integer), and blk = sum_k A[m,k] (q[k,n] - zp) over
+    // the group's k16 steps accumulates in fp32; then one fp32 multiply by the scale.
+    auto products = [&](const Frag &f, int g, float (&blk)[J][2][4]) {
       constexpr int kSteps = TWO_GROUPS ? 2 : 4;
+      uint32_t zsub[4];
+      if constexpr (HAS_ZP) {
+        magic_quad<BF>(prmt(f.zraw[g], 0u, 0x1010u), zsub);  // this quad's zero points in both halves
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) zsub[j] = zsym[j];
+      }
 #pragma unroll
       for (int tt = 0; tt < kSteps; ++tt) {
         const int t = g * kSteps + tt;
         uint32_t lo[4], hi[4];
         magic_quad<BF>(f.wq[2 * t], lo);
         magic_quad<BF>(f.wq[2 * t + 1], hi);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          lo[j] = sub2_rn<BF>(lo[j], zsub[j]);
+          hi[j] = sub2_rn<BF>(hi[j], zsub[j]);
+        }
         // MMA rows: g -> column 4*gl + j, g + 8 -> column 4*gl + j + 2, for j = 0 and j = 1
         const uint32_t a0[4] = {lo[0], lo[2], hi[0], hi[2]};
         const uint32_t a1[4] = {lo[1], lo[3], hi[1], hi[3]};
@@ -343,21 +345,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tt == 0) {
             mma_16816_z<BF>(blk[jt][0], a0, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
             mma_16816_z<BF>(blk[jt][1], a1, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
-            mma_16816_z<BF>(sa[jt], ones, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
           } else {
             mma_16816<BF>(blk[jt][0], a0, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
             mma_16816<BF>(blk[jt][1], a1, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
-            mma_16816<BF>(sa[jt], ones, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
           }
         }
       }
     };
-    auto scale_add = [&](const Frag &f, int g, const float (&blk)[J][2][4], const float (&sa)[J][4]) {
+    auto scale_add = [&](const Frag &f, int g, const float (&blk)[J][2][4]) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint32_t h = (j < 2 ? f.sraw[g][0] : f.sraw[g][1]) >> (16 * (j & 1));
         sc[j] = bits_to_f32<BF>(h & 0xFFFFu);
-        if constexpr (HAS_ZP) zc[j] = magic_base<BF>(j) + static_cast<float>((f.zraw[g] >> (4 * j)) & 0xFu);
       }
 #pragma unroll
       for (int jt = 0; jt < J; ++jt)
@@ -366,8 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j = q + 2 * (e >> 1);  // accumulator element e of MMA q holds column j
-            const float d = fmaf(-zc[j], sa[jt][e], blk[jt][q][e]);
-            acc[jt][q][e] = fmaf(sc[j], d, acc[jt][q][e]);
+            acc[jt][q][e] = fmaf(sc[j], blk[jt][q][e], acc[jt][q][e]);
           }
     };
     Frag f;
@@ -376,9 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 #pragma unroll
       for (int g = 0; g < kSRows; ++g) {
-        float blk[J][2][4], sa[J][4];
-        products(f, g, blk, sa);
-        scale_add(f, g, blk, sa);
+        float blk[J][2][4];
+        products(f, g, blk);
+        scale_add(f, g, blk);
       }
     }
   }
