@@ -11,7 +11,8 @@ is not part of a step.
 Default workload "decode_2112" (the non-128-aligned decode layers of the PR #43731 report's
 motivation): M in {1, 2, 4, 5, 8} x (K, N) in {(1152, 4224), (2112, 1152)}, G = 32, bf16,
 symmetric uint4b8, scales U[0.005, 0.02], A ~ N(0, 1). Metric: decode GB/s over the algorithmic bytes
-K*N/2 + 2(K/G)N [+ (K/G)N/2] + 2MK + 2MN [+ 2N] per call. "prefill" reports TFLOP/s (2MNK per call).
+K*N/2 + 2(K/G)N [+ (K/G)N/2] + 2MK + 2MN [+ 2N] per call. "prefill" reports TFLOP/s (2MNK per call);
+"mid_m" (17 <= M <= 64, served by the prefill kernel split over clusters) reports GB/s like decode.
 
 Timing: W eager warm-up steps through the C ABI, then exactly K steps replayed from CUDA graphs (the
 library's calls are capture-safe), bracketed by CUDA events on the launching stream, with a barrier
@@ -55,6 +56,8 @@ WORKLOADS = {
                  "fp16, asymmetric qzeros, fp16 bias N(0,0.1)",
     "prefill": "prefill: M in {512,1024,4096} x (K,N) in {(5120,34816),(17408,5120)}, G=64, bf16, "
                "asymmetric qzeros, scales U[0.002,0.01]",
+    "mid_m": "mid M: M in {17,24,32,64} x (K,N) in {(5120,7168),(17408,5120)}, G=128, bf16, symmetric "
+             "uint4b8, scales U[0.005,0.02], A~N(0,1)",
     "tiny": "tiny: M=4, K=256, N=512, G=128, fp16, symmetric",
 }
 
@@ -361,7 +364,7 @@ def run_cuda(args, rank, world, local_rank):
     else:
         # a kernel timed inside a long run of back-to-back steps: the sustained bf16 figure
         peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
-    dominant = "gemm_prefill" if name == "prefill" else "gemm_decode"
+    dominant = "gemm_prefill" if name in ("prefill", "mid_m") else "gemm_decode"
     achieved = value  # every launch in the timed region is the dominant kernel (see gpu_launches)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,

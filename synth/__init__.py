@@ -124,6 +124,10 @@ CONFIGS = {
     # prefill on a 27B-class decoder (PR #51453 report, motivation)
     "prefill": dict(Ms=[512, 1024, 4096], shapes=[(5120, 34816), (17408, 5120)], Gs=[64],
                     dtypes=["bf16"], asym=[True], bias=False, scale=(0.002, 0.01)),
+    # mid M on two of the same 27B-class layers: one 128-row tile per column tile, K split over a
+    # thread-block cluster (weight bytes still dominate the roofline up to M = 64)
+    "mid_m": dict(Ms=[17, 24, 32, 64], shapes=[(5120, 7168), (17408, 5120)], Gs=[128],
+                  dtypes=["bf16"], asym=[False], bias=False, scale=(0.005, 0.02)),
     # full M sweep on the same 27B-class layer
     "sweep": dict(Ms=[1, 2, 4, 5, 6, 8, 16, 24, 32, 64, 128, 256, 512, 1024, 2048, 4096, 8192],
                   shapes=[(5120, 7168), (5120, 34816), (17408, 5120)], Gs=[128, "K"],
