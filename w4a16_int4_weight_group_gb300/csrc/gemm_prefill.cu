@@ -63,6 +63,10 @@ struct PLayout {
   static constexpr int SA = MT == 1 ? 5 : 3;   // stages of A
   static constexpr int SP = kShared ? SA : 3;  // stages of packed weights / scales / zeros
   static constexpr int SB = 3;                 // stages of dequantised weights
+  // MT = 1: the dequantisers work in two groups of 4 warps on alternate K blocks (a group's waits,
+  // fence and arrivals overlap the other group's arithmetic); MT = 2: all 8 warps on every block.
+  static constexpr int kDqGroups = MT == 1 ? 2 : 1;
+  static constexpr int kGroupWarps = kDequantWarps / kDqGroups;
   static constexpr uint32_t kTmemCols = 256u * MT;
   static constexpr int kABytes = BM * BK * 2;        // 16 KB per 128 rows
   static constexpr int kPBytes = BK * (BN / 8) * 4;  // 8 KB
@@ -206,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = PLayout<MT>;
   constexpr int BM = L::BM, SA = L::SA, SB = L::SB, SP = L::SP;
   constexpr bool kShared = L::kShared;
+  constexpr int kDqGroups = L::kDqGroups, kGroupWarps = L::kGroupWarps;
   constexpr int kABytes = L::kABytes, kPBytes = L::kPBytes, kSBytes = L::kSBytes, kZBytes = L::kZBytes,
                 kBBytes = L::kBBytes;
   constexpr int kOffA = L::kOffA, kOffB = L::kOffB, kOffP = L::kOffP, kOffS = L::kOffS, kOffZ = L::kOffZ,
@@ -271,16 +276,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; ++s) {
       mbar_init(full_a(s), 1);
-      mbar_init(empty_a(s), kShared ? kDequantWarps + 1 : 1);  // shared: the dequantisers and the MMAs
+      mbar_init(empty_a(s), kShared ? kGroupWarps + 1 : 1);  // shared: the dequantisers and the MMAs
     }
     if constexpr (!kShared) {
       for (int s = 0; s < SP; ++s) {
         mbar_init(full_p(s), 1);
-        mbar_init(empty_p(s), kDequantWarps);
+        mbar_init(empty_p(s), kGroupWarps);
       }
     }
     for (int s = 0; s < SB; ++s) {
-      mbar_init(full_b(s), kDequantWarps);
+      mbar_init(full_b(s), kGroupWarps);
       mbar_init(empty_b(s), 1);
     }
     mbar_init(accum_full, 1);
@@ -496,58 +501,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int64_t t = t_first;
     int kb = kb_first, seg = 0, seg_kb0 = kb_first, epi_uses = 0;
+    const int dgrp = dw / kGroupWarps, dwg = dw % kGroupWarps;  // dequantiser group, warp within it
     for (int i = 0; i < n_units && ok; ++i) {
-      const int sp = i % SP, sb = i % SB;
-      ok = wait_phase(full_p(sp), (i / SP) & 1, abort_flag, limit_ns, &g_prefill_error) &&
-           wait_phase(empty_b(sb), ((i / SB) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error);
-      ok = __all_sync(0xffffffffu, ok);  // the warp leaves the loop together
-      if (!ok) break;
-      const uint32_t P = base + kOffP + sp * kPBytes;
-      const uint32_t S = base + kOffS + sp * kSBytes;
-      const uint32_t Z = base + kOffZ + sp * kZBytes;
-      const uint32_t B = base + kOffB + sb * kBBytes;
-      // every shared-memory load of the block first (independent, so their latencies overlap), then
-      // the arithmetic and the stores
-      constexpr int kRows = BK / kDequantWarps;  // rows dw, dw + 8, ... of the block
-      uint32_t sw[2][4], zw[2], wq[kRows];
+      if (i % kDqGroups == dgrp) {
+        const int sp = i % SP, sb = i % SB;
+        ok = wait_phase(full_p(sp), (i / SP) & 1, abort_flag, limit_ns, &g_prefill_error) &&
+             wait_phase(empty_b(sb), ((i / SB) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error);
+        ok = __all_sync(0xffffffffu, ok);  // the warp leaves the loop together
+        if (!ok) break;
+        const uint32_t P = base + kOffP + sp * kPBytes;
+        const uint32_t S = base + kOffS + sp * kSBytes;
+        const uint32_t Z = base + kOffZ + sp * kZBytes;
+        const uint32_t B = base + kOffB + sb * kBBytes;
+        // every shared-memory load of the block first (independent, so their latencies overlap), then
+        // the arithmetic and the stores
+        constexpr int kRows = BK / kGroupWarps;  // rows dwg, dwg + kGroupWarps, ... of the block
+        uint32_t sw[2][4], zw[2], wq[kRows];
 #pragma unroll
-      for (int gr = 0; gr < srows; ++gr) {
-        lds128(S + gr * (BN * 2) + c * 16, sw[gr][0], sw[gr][1], sw[gr][2], sw[gr][3]);
-        if constexpr (HAS_ZP) zw[gr] = lds32(Z + gr * (BN / 2) + c * 4);
-      }
-#pragma unroll
-      for (int ii = 0; ii < kRows; ++ii) wq[ii] = lds32(P + (dw + kDequantWarps * ii) * (BN / 2) + c * 4);
-      // the weight slot is free once every lane's loads have been performed (shared-memory accesses
-      // of a warp complete in order, ahead of the arrive)
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_p(sp));
-#pragma unroll
-      for (int gr = 0; gr < srows; ++gr) {
-        spair[gr][0] = prmt(sw[gr][0], sw[gr][2], 0x5410);  // (s0, s4)
-        spair[gr][1] = prmt(sw[gr][0], sw[gr][2], 0x7632);  // (s1, s5)
-        spair[gr][2] = prmt(sw[gr][1], sw[gr][3], 0x5410);  // (s2, s6)
-        spair[gr][3] = prmt(sw[gr][1], sw[gr][3], 0x7632);  // (s3, s7)
-        if constexpr (HAS_ZP) magic4<BF>(zw[gr], zsub[gr]);
-      }
-#pragma unroll
-      for (int ii = 0; ii < kRows; ++ii) {
-        const int r = dw + kDequantWarps * ii;
-        const int gr = (TWO_GROUPS && ii >= kRows / 2) ? 1 : 0;  // rows 32..63: second group
-        uint32_t h[4];
-        magic4<BF>(wq[ii], h);
-        uint32_t x[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          x[j] = mul2_rn<BF>(sub2_rn<BF>(h[j], zsub[gr][j]), spair[gr][j]);
+        for (int gr = 0; gr < srows; ++gr) {
+          lds128(S + gr * (BN * 2) + c * 16, sw[gr][0], sw[gr][1], sw[gr][2], sw[gr][3]);
+          if constexpr (HAS_ZP) zw[gr] = lds32(Z + gr * (BN / 2) + c * 4);
         }
-        // MN-major, 128-byte swizzle: 8-row K groups 4096 B apart, 64-column atoms 1024 B apart,
-        // row r%8 at 128 B, 16-byte chunk (c%8) XOR (r%8).
-        const uint32_t off = (r >> 3) * 4096u + (c >> 3) * 1024u + (r & 7) * 128u + ((((c & 7) ^ (r & 7))) << 4);
-        sts128(B + off, x[0], x[1], x[2], x[3]);
+#pragma unroll
+        for (int ii = 0; ii < kRows; ++ii) wq[ii] = lds32(P + (dwg + kGroupWarps * ii) * (BN / 2) + c * 4);
+        // the weight slot is free once every lane's loads have been performed (shared-memory accesses
+        // of a warp complete in order, ahead of the arrive)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_p(sp));
+#pragma unroll
+        for (int gr = 0; gr < srows; ++gr) {
+          spair[gr][0] = prmt(sw[gr][0], sw[gr][2], 0x5410);  // (s0, s4)
+          spair[gr][1] = prmt(sw[gr][0], sw[gr][2], 0x7632);  // (s1, s5)
+          spair[gr][2] = prmt(sw[gr][1], sw[gr][3], 0x5410);  // (s2, s6)
+          spair[gr][3] = prmt(sw[gr][1], sw[gr][3], 0x7632);  // (s3, s7)
+          if constexpr (HAS_ZP) magic4<BF>(zw[gr], zsub[gr]);
+        }
+#pragma unroll
+        for (int ii = 0; ii < kRows; ++ii) {
+          const int r = dwg + kGroupWarps * ii;
+          const int gr = (TWO_GROUPS && ii >= kRows / 2) ? 1 : 0;  // rows 32..63: second group
+          uint32_t h[4];
+          magic4<BF>(wq[ii], h);
+          uint32_t x[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            x[j] = mul2_rn<BF>(sub2_rn<BF>(h[j], zsub[gr][j]), spair[gr][j]);
+          }
+          // MN-major, 128-byte swizzle: 8-row K groups 4096 B apart, 64-column atoms 1024 B apart,
+          // row r%8 at 128 B, 16-byte chunk (c%8) XOR (r%8).
+          const uint32_t off = (r >> 3) * 4096u + (c >> 3) * 1024u + (r & 7) * 128u + ((((c & 7) ^ (r & 7))) << 4);
+          sts128(B + off, x[0], x[1], x[2], x[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full_b(sb));
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(full_b(sb));
 
       const bool seg_end = (kb == nk - 1) || (i == n_units - 1);
       if (seg_end) {
