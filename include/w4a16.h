@@ -122,7 +122,7 @@ w4a16_status w4a16_repack_k_to_n(const int32_t *k_packed, int32_t *b_q, int64_t 
  * i.e. the exact product rounded once to nearest-even (dequantisation rule: PR #40977 report, key
  * source snippets, test reference; zp = qzeros nibble, or zp_bias when qzeros is NULL). The prefill
  * kernel feeds exactly these values to its tensor-core MMA; the decode kernel multiplies the exact
- * integers and applies the scale in fp32, so a one-hot activation row reproduces them exactly too.
+ * integers q - zp and applies the scale in fp32, so a one-hot activation row reproduces them exactly.
  *   b_q [k, n/8] int32, scales [k/G, n] dtype, qzeros [k/G, n/8] int32 or NULL, w_out [k, n] dtype.
  * Errors: as w4a16_gemm's validation (dtype, n % 8, group size, k % G, zp_bias, nulls, overlap).
  */
