@@ -159,9 +159,12 @@ w4a16_status w4a16_gemm(const void *a, const int32_t *b_q, const void *scales, c
  * the (tile, K block) work and exchange fp32 partial tiles through the workspace.
  *   workspace       device memory, 256-byte aligned, at least w4a16_gemm_workspace_size(...) bytes
  *                   (a smaller or NULL workspace simply disables stream-K). Its first 4 KiB hold
- *                   per-CTA flags: they must be zero before the first use, and every call leaves
- *                   them zero again; the rest is scratch whose contents between calls do not matter
- *                   (zero-filling the whole buffer once is the simple way to satisfy this)
+ *                   per-CTA flags: they must be zero before the first use, and every call that
+ *                   completes leaves them zero again; the rest is scratch whose contents between
+ *                   calls do not matter (zero-filling the whole buffer once is the simple way to
+ *                   satisfy this). A call that gives up a bounded wait (w4a16_get_device_error then
+ *                   reports W4A16_ERR_TIMEOUT) may leave flags set: zero the first 4 KiB again before
+ *                   the workspace is used by another call.
  *   workspace_bytes its size
  * Calls that may run concurrently (different streams) need different workspaces. Everything else
  * is as for w4a16_gemm (no allocation, no synchronisation, no host read).
@@ -200,6 +203,32 @@ w4a16_status w4a16_gemm_noalloc(const void *a, const int32_t *b_q, const void *s
 size_t w4a16_gemm_workspace_size(int64_t m, int64_t k, int64_t n, int group_size, int dtype);
 
 /*
+ * Prepared layer: the weights of one linear layer checked once, and per call shape the dispatcher's
+ * plan and the TMA descriptors of the weights kept, so that a call (a model's per-layer, per-step
+ * call) checks and encodes only the activations and the output. The handle stores the weight
+ * pointers, not copies: the caller keeps b_q, scales, qzeros and bias alive and unchanged while the
+ * handle is in use. It is bound to the device current at creation. A handle may be used from
+ * several threads (an internal lock guards its cache).
+ *
+ * w4a16_layer_create - validates the layer configuration as w4a16_gemm does (dtype, n % 8, group
+ *   size, k % G, zp_bias, NULL b_q / scales, natural alignment) and returns a handle in *layer.
+ *   Host memory only; no device access. Errors: those of the validation.
+ * w4a16_layer_gemm - out[m, n] = w4a16_gemm(a, layer weights, ...) with an optional workspace as in
+ *   w4a16_gemm_ws (NULL: none). Same results, launches and errors as w4a16_gemm / w4a16_gemm_ws, plus
+ *   INVALID_ARG when the current device is not the layer's.
+ * w4a16_layer_workspace_size - w4a16_gemm_workspace_size for this layer and m.
+ * w4a16_layer_destroy - releases the handle (NULL is allowed); the weights are not touched.
+ */
+typedef struct w4a16_layer_st *w4a16_layer_t;
+w4a16_status w4a16_layer_create(const int32_t *b_q, const void *scales, const int32_t *qzeros, int group_size,
+                                int zp_bias, const void *bias, int64_t k, int64_t n, w4a16_dtype dtype,
+                                w4a16_layer_t *layer);
+w4a16_status w4a16_layer_gemm(w4a16_layer_t layer, const void *a, void *out, int64_t m, void *workspace,
+                              size_t workspace_bytes, w4a16_stream_t stream);
+size_t w4a16_layer_workspace_size(w4a16_layer_t layer, int64_t m);
+w4a16_status w4a16_layer_destroy(w4a16_layer_t layer);
+
+/*
  * w4a16_can_implement - host-only check of a layer configuration, mirroring
  * TritonW4A16LinearKernel.can_implement (PR #43731 report, key source snippets): returns W4A16_OK or
  * the rejection status, with the reason available from w4a16_last_error(). No device access.
@@ -227,6 +256,16 @@ w4a16_status w4a16_get_device_error(void);
 
 /* Path w4a16_gemm would choose for these sizes on the current device (a w4a16_path value), or -1. */
 int w4a16_debug_selected_path(int64_t m, int64_t k, int64_t n, int group_size);
+
+/*
+ * w4a16_debug_force_path - restricts the dispatcher to one path for tests and benchmarks:
+ * W4A16_PATH_GENERIC, W4A16_PATH_DECODE or W4A16_PATH_PREFILL (used when that path supports the call,
+ * otherwise the dispatcher chooses as usual), or -1 to lift the restriction. The initial value comes
+ * from the environment variable W4A16_FORCE_PATH (generic|decode|prefill), read once at the first
+ * call that plans. Process-wide; not meant for concurrent use with calls on other threads.
+ * Errors: INVALID_ARG for any other value.
+ */
+w4a16_status w4a16_debug_force_path(int path);
 
 /*
  * w4a16_debug_set_wait_limit_ns - sets the limit of every bounded device-side wait (nanoseconds;

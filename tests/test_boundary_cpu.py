@@ -186,3 +186,24 @@ def test_prepared_layer_rejects_host_tensors(w):
         w.W4A16Linear(b_q, scales, None, 128)
     with pytest.raises(ValueError):
         w.W4A16Linear(b_q.to(torch.int64), scales, None, 128)
+
+
+def test_layer_handle_validation_without_a_device(w):
+    """The prepared-layer entry points reject bad configurations and a NULL handle before touching
+    any device."""
+    L = w.lib()
+    h = ctypes.c_void_p()
+    assert L.w4a16_layer_create(0x1000, 0x2000, None, 128, 8, None, 256, 516, 0, ctypes.byref(h)) == 1
+    assert "divisible by 8" in w.last_error() and h.value is None
+    assert L.w4a16_layer_create(0x1000, 0x2000, None, 96, 8, None, 256, 512, 0, ctypes.byref(h)) == 2
+    assert L.w4a16_layer_create(0x1000, 0x2000, None, 128, 16, None, 256, 512, 0, ctypes.byref(h)) == 1
+    assert L.w4a16_layer_create(None, 0x2000, None, 128, 8, None, 256, 512, 0, ctypes.byref(h)) == 1
+    assert L.w4a16_layer_create(0x1001, 0x2000, None, 128, 8, None, 256, 512, 0, ctypes.byref(h)) == 3
+    assert L.w4a16_layer_gemm(None, 0x1000, 0x2000, 4, None, 0, None) == 1 and "layer" in w.last_error()
+    assert L.w4a16_layer_workspace_size(None, 4) == 0
+    assert L.w4a16_layer_destroy(None) == 0
+
+
+def test_force_path_entry_point_validates(w):
+    assert w.lib().w4a16_debug_force_path(7) == 1
+    assert w.lib().w4a16_debug_force_path(-1) == 0

@@ -11,8 +11,8 @@ import torch
 
 import oracle
 import synth
-from tests._util import (bits_to_torch, case_tensors, check_against_oracle, forced_path, sample_cols,
-                         torch_to_bits)
+from tests._util import (bits_to_torch, case_tensors, check_against_oracle, forced_path, path_taken,
+                         sample_cols, torch_to_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -99,7 +99,7 @@ def test_gemm_matches_oracle_every_path(w, case):
     outs = {}
     for p in paths + [None]:
         outs[p] = run(w, c, p)
-        check_against_oracle(c, outs[p], label=f"path={p or auto}")
+        check_against_oracle(c, outs[p], label=f"path={p or auto}", path=p or auto)
     # the automatic choice is one of the checked paths and gives the same bits as forcing it
     assert np.array_equal(outs[None], outs[auto])
 
@@ -153,21 +153,21 @@ def test_unaligned_pointers_take_the_generic_path(w):
     a2.copy_(t["a"])
     out = w.w4a16_gemm(a2, t["b_q"], t["scales"], t["qzeros"], c.G, 8, t["bias"])
     torch.cuda.synchronize()
-    check_against_oracle(c, torch_to_bits(out), label="unaligned a")
+    check_against_oracle(c, torch_to_bits(out), label="unaligned a", path="generic")
 
 
 @pytest.mark.parametrize("zp", [0, 15])
 def test_zp_bias_values(w, zp):
     c = synth.make_case(3, 512, 512, 64, "f16", seed=zp, zp_bias=zp)
     for p in supported_paths(w, c)[0]:
-        check_against_oracle(c, run(w, c, p), label=f"zp_bias={zp} path={p}")
+        check_against_oracle(c, run(w, c, p), label=f"zp_bias={zp} path={p}", path=p)
 
 
 def test_dispatch_threshold_neighbours(w):
     # every switch point of the dispatcher, +-1
     for M in (1, 8, 9, 16, 17, 64, 65, 128, 129):
         c = synth.make_case(M, 512, 1024, 128, "bf16", asym=True, seed=M)
-        check_against_oracle(c, run(w, c), label=f"M={M}")
+        check_against_oracle(c, run(w, c), label=f"M={M}", path=path_taken(w, c))
 
 
 # ------------------------------------------------------------------------------------------------
@@ -183,7 +183,7 @@ def _config_ids(name):
 def test_decode_workloads_full_output(w, args):
     M, K, N, G, dt, asym, bias, lo, hi, seed = args
     c = synth.make_case(M, K, N, G, dt, asym=asym, bias=bias, seed=seed, scale_lo=lo, scale_hi=hi)
-    check_against_oracle(c, run(w, c), label="full")
+    check_against_oracle(c, run(w, c), label="full", path=path_taken(w, c))
 
 
 @pytest.mark.parametrize("args", list(synth.config_cases("decode_4b")), ids=_config_ids("decode_4b"))
@@ -192,7 +192,7 @@ def test_decode_4b_workload_sampled_columns(w, args):
     c = synth.make_case(M, K, N, G, dt, asym=asym, bias=bias, seed=seed, scale_lo=lo, scale_hi=hi)
     out = run(w, c)
     cols = sample_cols(N, np.random.default_rng(seed))
-    check_against_oracle(c, out, cols=cols, label="sampled")
+    check_against_oracle(c, out, cols=cols, label="sampled", path=path_taken(w, c))
 
 
 @pytest.mark.parametrize("args", list(synth.config_cases("prefill")), ids=_config_ids("prefill"))
@@ -205,20 +205,30 @@ def test_prefill_workload_sampled(w, args):
     rng = np.random.default_rng(seed)
     rows = sorted({0, 1, 127, 128, M // 2, M - 1} | set(rng.integers(0, M, size=4).tolist()))
     cols = sample_cols(N, rng, k=128)
-    check_against_oracle(c, out, rows=rows, cols=cols, label="prefill sampled")
+    check_against_oracle(c, out, rows=rows, cols=cols, label="prefill sampled", path="prefill")
 
 
-@pytest.mark.parametrize("M,K,N,G", [(1024, 5120, 7168, 128), (256, 17408, 512, 17408), (24, 5120, 7168, 128),
-                                     (64, 17408, 5120, 17408), (16, 5120, 34816, 128)])
-def test_sweep_shapes_sampled(w, M, K, N, G):
-    """27B-class layer shapes of the M sweep, per-group and per-channel scales; the mid-M sizes run
-    stream-K over 128-row tiles, M = 16 the two-accumulator-set decode kernel."""
-    for dt, asym in (("f16", False), ("bf16", True)):
-        c = synth.make_case(M, K, N, G, dt, asym=asym, seed=M + G)
-        out = run(w, c)
-        rng = np.random.default_rng(M)
-        rows = sorted({0, M - 1} | set(rng.integers(0, M, size=4).tolist()))
-        check_against_oracle(c, out, rows=rows, cols=sample_cols(N, rng, k=128), label=f"{dt} {asym}")
+# The full M sweep on the 27B-class layers: every M of the sweep with every (dtype, group size,
+# zero-point) variant on 5120 -> 7168, and the largest M on the other two layers.
+_SWEEP_VARIANTS = [(dt, g, asym) for dt in ("f16", "bf16") for g in (128, "K") for asym in (False, True)]
+SWEEP_CASES = ([(M, 5120, 7168, g, dt, asym) for M in synth.CONFIGS["sweep"]["Ms"] for (dt, g, asym) in _SWEEP_VARIANTS]
+               + [(8192, K, N, g, dt, asym) for (K, N) in ((5120, 34816), (17408, 5120))
+                  for (dt, g, asym) in (("f16", 128, True), ("bf16", "K", False))]
+               + [(M, 17408, 5120, "K", "bf16", True) for M in (16, 64, 256, 2048)])
+
+
+@pytest.mark.parametrize("M,K,N,g,dt,asym", SWEEP_CASES, ids=[
+    f"M{M}-K{K}-N{N}-G{g}-{dt}-{'asym' if asym else 'sym'}" for (M, K, N, g, dt, asym) in SWEEP_CASES])
+def test_sweep_shapes_sampled(w, M, K, N, g, dt, asym):
+    """Sampled rows (first, last, random) and columns (both edges, every n % 8, random) of each sweep
+    case, through the path the dispatcher picks for it, against the oracle."""
+    G = K if g == "K" else g
+    c = synth.make_case(M, K, N, G, dt, asym=asym, seed=M + G + (1 if asym else 0))
+    out = run(w, c)
+    rng = np.random.default_rng(M)
+    rows = sorted({0, M - 1} | set(rng.integers(0, M, size=4).tolist()))
+    check_against_oracle(c, out, rows=rows, cols=sample_cols(N, rng, k=128), label=f"{dt} {'asym' if asym else 'sym'}",
+                         path=path_taken(w, c))
 
 
 @pytest.mark.parametrize("M,K,N,G,dt,asym", [(512, 4096, 1024, 128, "bf16", True), (300, 2048, 768, 64, "f16", False),
@@ -250,11 +260,12 @@ def test_stream_k_matches_oracle_and_leaves_workspace_clean(w, M, K, N, G, dt, a
     assert int(flags.count_nonzero()) == 0, "flags must be left zero"
     rng = np.random.default_rng(M)
     rows = sorted({0, M - 1} | set(rng.integers(0, M, size=6).tolist()))
-    check_against_oracle(c, outs[0], rows=rows, cols=sample_cols(N, rng, k=128), label="stream-K")
+    check_against_oracle(c, outs[0], rows=rows, cols=sample_cols(N, rng, k=128), label="stream-K", path="prefill")
     # the same call without a workspace (whole tiles per CTA) agrees within the tolerance too
     out2 = w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"], use_workspace=False)
     torch.cuda.synchronize()
-    check_against_oracle(c, torch_to_bits(out2), rows=rows, cols=sample_cols(N, rng, k=64), label="no workspace")
+    check_against_oracle(c, torch_to_bits(out2), rows=rows, cols=sample_cols(N, rng, k=64), label="no workspace",
+                         path=path_taken(w, c, with_workspace=False))
 
 
 @pytest.mark.parametrize("shift", [0, 8])
@@ -272,7 +283,7 @@ def test_prefill_output_alignment_paths(w, shift):
     assert w.w4a16_plan(M, K, N, G, 1, True, 0)["path_name"] == "prefill"
     rng = np.random.default_rng(shift)
     check_against_oracle(c, torch_to_bits(out), rows=np.arange(0, M, 13), cols=sample_cols(N, rng, k=64),
-                         label=f"out shifted by {shift}")
+                         label=f"out shifted by {shift}", path="prefill")
 
 
 @pytest.mark.parametrize("K,N", [(8, 8), (2112, 1152), (1152, 4224), (4104, 264)])
@@ -288,18 +299,52 @@ def test_repack_k_to_n_bitexact(w, K, N):
 
 
 
-@pytest.mark.parametrize("M,K,N,G,dt,asym", [(1, 2112, 1152, 32, "bf16", False), (300, 2048, 768, 64, "f16", True)])
+@pytest.mark.parametrize("M,K,N,G,dt,asym", [(1, 2112, 1152, 32, "bf16", False), (8, 2560, 3840, 128, "f16", True),
+                                           (300, 2048, 768, 64, "f16", True), (40, 5120, 7168, 128, "bf16", False),
+                                           (512, 4096, 1024, 128, "bf16", True), (7, 100, 520, 100, "f16", True)])
 def test_prepared_layer_equals_the_function(w, M, K, N, G, dt, asym):
-    """W4A16Linear (weights checked once) gives exactly what w4a16_gemm gives, decode and prefill."""
+    """W4A16Linear (the library's prepared-layer handle: weights checked once, plan and weight
+    descriptors kept per shape) gives exactly what w4a16_gemm gives on every path, and repeated
+    calls with other activations and another M reuse the handle correctly."""
     c = synth.make_case(M, K, N, G, dt, asym=asym, bias=True, seed=5)
     t = case_tensors(c)
     layer = w.W4A16Linear(t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"])
-    got = layer(t["a"])
-    want = w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"])
-    torch.cuda.synchronize()
-    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    for m in (M, max(1, M // 2), M):
+        a = t["a"][:m].contiguous() if m != M else t["a"]
+        a2 = (a * 0.5).contiguous()
+        for x in (a, a2):
+            got = layer(x)
+            want = w.w4a16_gemm(x, t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"])
+            torch.cuda.synchronize()
+            assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"m={m}"
     with pytest.raises(ValueError):
         layer(t["a"][:, :8].contiguous())  # wrong K
+
+
+def test_layer_handle_through_the_c_abi(w):
+    """w4a16_layer_create / _gemm / _workspace_size / _destroy called directly through the C ABI."""
+    import ctypes
+    M, K, N, G = 512, 4096, 1024, 128
+    c = synth.make_case(M, K, N, G, "bf16", asym=True, bias=True, seed=9)
+    t = case_tensors(c)
+    L = w.lib()
+    h = ctypes.c_void_p()
+    assert L.w4a16_layer_create(t["b_q"].data_ptr(), t["scales"].data_ptr(), t["qzeros"].data_ptr(), G, 8,
+                                t["bias"].data_ptr(), K, N, 1, ctypes.byref(h)) == 0, w.last_error()
+    need = L.w4a16_layer_workspace_size(h, M)
+    assert need == w.w4a16_gemm_workspace_size(M, K, N, G, 1) and need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    assert L.w4a16_layer_gemm(h, t["a"].data_ptr(), out.data_ptr(), M, ws.data_ptr(), need, None) == 0, w.last_error()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1)
+    check_against_oracle(c, torch_to_bits(out), rows=np.arange(0, M, 41), cols=sample_cols(N, rng, k=64),
+                         label="layer handle", path="prefill")
+    # out overlapping the activations is rejected before any launch
+    before = w.w4a16_debug_launch_count()
+    assert L.w4a16_layer_gemm(h, t["a"].data_ptr(), t["a"].data_ptr(), M, None, 0, None) == 1
+    assert w.w4a16_debug_launch_count() == before
+    assert L.w4a16_layer_destroy(h) == 0
 
 
 def test_plans_of_different_shapes_share_one_workspace(w):
@@ -328,7 +373,7 @@ def test_plans_of_different_shapes_share_one_workspace(w):
             torch.cuda.synchronize()
             rows = np.unique(np.linspace(0, c.M - 1, 5).astype(int))
             check_against_oracle(c, torch_to_bits(out), rows=rows, cols=sample_cols(c.N, rng, k=32),
-                                 label=f"round {rnd} M={c.M}")
+                                 label=f"round {rnd} M={c.M}", path="prefill")
 
 
 @pytest.mark.parametrize("M,K,N,G,dt,asym", [(40, 5120, 7168, 128, "f16", True), (100, 2112, 1152, 32, "bf16", False),
@@ -350,5 +395,6 @@ def test_cluster_split_k_mid_m(w, M, K, N, G, dt, asym):
     assert w.w4a16_get_device_error() == 0
     rng = np.random.default_rng(M)
     rows = sorted({0, M - 1} | set(rng.integers(0, M, size=6).tolist()))
-    check_against_oracle(c, outs[0], rows=rows, cols=sample_cols(N, rng, k=128), label="cluster split-K")
+    check_against_oracle(c, outs[0], rows=rows, cols=sample_cols(N, rng, k=128), label="cluster split-K",
+                         path="prefill")
 

@@ -55,6 +55,11 @@ SIGNATURES = [
     ("w4a16_gemm_ws", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_int, _vp,
                                ctypes.c_size_t, _vp]),
     ("w4a16_gemm_workspace_size", ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_int, _c_int]),
+    ("w4a16_layer_create", _c_int, [_vp, _vp, _vp, _c_int, _c_int, _vp, _c_i64, _c_i64, _c_int,
+                                    ctypes.POINTER(_vp)]),
+    ("w4a16_layer_gemm", _c_int, [_vp, _vp, _vp, _c_i64, _vp, ctypes.c_size_t, _vp]),
+    ("w4a16_layer_workspace_size", ctypes.c_size_t, [_vp, _c_i64]),
+    ("w4a16_layer_destroy", _c_int, [_vp]),
     ("w4a16_gemm_noalloc", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_int,
                                     _vp]),
     ("w4a16_can_implement", _c_int, [_c_i64, _c_i64, _c_int, _c_int, _c_int]),
@@ -62,6 +67,7 @@ SIGNATURES = [
     ("w4a16_last_error", ctypes.c_char_p, []),
     ("w4a16_get_device_error", _c_int, []),
     ("w4a16_debug_selected_path", _c_int, [_c_i64, _c_i64, _c_i64, _c_int]),
+    ("w4a16_debug_force_path", _c_int, [_c_int]),
     ("w4a16_debug_set_wait_limit_ns", _c_int, [ctypes.c_uint64]),
     ("w4a16_debug_inject_stall", _c_int, [_c_int]),
     ("w4a16_debug_launch_count", ctypes.c_uint64, []),
@@ -249,9 +255,10 @@ def w4a16_gemm(a: torch.Tensor, b_q: torch.Tensor, scales: torch.Tensor, qzeros:
 class W4A16Linear:
     """A prepared W4A16 layer: out[M, N] = a[M, K] @ dequant(W) (+ bias), as w4a16_gemm.
 
-    The weights (b_q, scales, qzeros or zp_bias, bias) are checked once, when the layer is built;
-    each call checks only the activations and the output, so the host work per call is small (decode
-    calls take a few microseconds on the GPU). The layer keeps references to its tensors.
+    Wraps the library's prepared-layer handle (w4a16_layer_create): the weights (b_q, scales, qzeros or
+    zp_bias, bias) are checked once, and the dispatcher's plan and the weight descriptors are kept per
+    call shape inside the library, so each call checks and encodes only the activations and the output.
+    The layer keeps references to its tensors (the handle stores their pointers).
     """
 
     def __init__(self, b_q: torch.Tensor, scales: torch.Tensor, qzeros: Optional[torch.Tensor], group_size: int,
@@ -262,6 +269,7 @@ class W4A16Linear:
             raise ValueError("qzeros must be int32")
         if bias is not None and bias.dtype != scales.dtype:
             raise ValueError("bias must have the dtype of scales")
+        self._handle = None
         self.device = _require_cuda(b_q, scales, qzeros, bias)
         self.k, self.n = b_q.shape[0], b_q.shape[1] * 8
         self.dtype = scales.dtype
@@ -269,9 +277,22 @@ class W4A16Linear:
         self.group_size, self.zp_bias = int(group_size), int(zp_bias)
         self.use_workspace = use_workspace
         self._tensors = (b_q, scales, qzeros, bias)
-        self._ptrs = (_ptr(b_q), _ptr(scales), _ptr(qzeros))
-        self._bias = _ptr(bias)
         self._need = {}
+        L = lib()
+        h = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            _check(L.w4a16_layer_create(b_q.data_ptr(), scales.data_ptr(), None if qzeros is None else qzeros.data_ptr(),
+                                        self.group_size, self.zp_bias, None if bias is None else bias.data_ptr(),
+                                        self.k, self.n, self.code, ctypes.byref(h)))
+        self._handle = h.value
+        self._lib = L
+        self._gemm = L.w4a16_layer_gemm
+
+    def __del__(self):
+        h = getattr(self, "_handle", None)
+        if h and _lib is not None:
+            _lib.w4a16_layer_destroy(h)
+            self._handle = None
 
     def __call__(self, a: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
         if (a.dim() != 2 or a.shape[1] != self.k or a.dtype != self.dtype or a.device != self.device
@@ -284,19 +305,18 @@ class W4A16Linear:
               or not out.is_contiguous()):
             raise ValueError(f"out must be a contiguous [{m}, {self.n}] {self.dtype} tensor on {self.device}")
         stream = _stream(self.device)
-        L = lib()
         need = 0
         if self.use_workspace:
             need = self._need.get(m)
             if need is None:
-                need = self._need[m] = int(L.w4a16_gemm_workspace_size(m, self.k, self.n, self.group_size, self.code))
+                need = self._need[m] = int(self._lib.w4a16_layer_workspace_size(self._handle, m))
         if need:
             ws = workspace_for(self.device, stream.value or 0, need)
-            _check(L.w4a16_gemm_ws(_ptr(a), *self._ptrs, self.group_size, self.zp_bias, self._bias, _ptr(out), m,
-                                   self.k, self.n, self.code, _ptr(ws), ws.numel(), stream))
+            st = self._gemm(self._handle, a.data_ptr(), out.data_ptr(), m, ws.data_ptr(), ws.numel(), stream)
         else:
-            _check(L.w4a16_gemm(_ptr(a), *self._ptrs, self.group_size, self.zp_bias, self._bias, _ptr(out), m,
-                                self.k, self.n, self.code, stream))
+            st = self._gemm(self._handle, a.data_ptr(), out.data_ptr(), m, None, 0, stream)
+        if st != 0:
+            raise W4A16Error(st, last_error())
         return out
 
 
@@ -322,11 +342,25 @@ def w4a16_gemm_workspace_size(m: int, k: int, n: int, group_size: int, dtype=W4A
 
 
 def w4a16_get_device_error() -> int:
-    return lib().w4a16_get_device_error()
+    """The library's device-side error status (read and cleared). After a TIMEOUT a stream-K call may
+    have stopped with partial-tile flags still set in its workspace, so the flag area of every
+    workspace this module keeps is zeroed again before any further call can use it."""
+    st = lib().w4a16_get_device_error()
+    if st == 5:
+        for buf in _workspaces.values():
+            buf[:4096].zero_()
+        torch.cuda.synchronize()
+    return st
 
 
 def w4a16_debug_selected_path(m: int, k: int, n: int, group_size: int) -> int:
     return lib().w4a16_debug_selected_path(m, k, n, group_size)
+
+
+def w4a16_debug_force_path(path):
+    """Restrict the dispatcher to a path ("generic", "decode", "prefill"), or lift it (None)."""
+    code = {None: -1, "generic": 1, "decode": 2, "prefill": 3}[path]
+    _check(lib().w4a16_debug_force_path(code))
 
 
 def w4a16_debug_set_wait_limit_ns(ns: int):
@@ -347,7 +381,8 @@ def w4a16_version() -> str:
 
 __all__ = ["w4a16_pack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_can_implement", "w4a16_plan",
            "w4a16_gemm_workspace_size", "workspace_for",
-           "w4a16_get_device_error", "w4a16_debug_selected_path", "w4a16_debug_set_wait_limit_ns",
+           "w4a16_get_device_error", "w4a16_debug_selected_path", "w4a16_debug_force_path",
+           "w4a16_debug_set_wait_limit_ns",
            "w4a16_debug_inject_stall",
            "w4a16_debug_launch_count", "w4a16_version", "W4A16Error", "lib", "last_error", "LIB_PATH",
            "SIGNATURES", "PATHS"]

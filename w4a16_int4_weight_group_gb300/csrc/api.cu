@@ -13,6 +13,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <unordered_map>
 
 #include "internal.h"
 
@@ -76,14 +77,21 @@ w4a16_status check_config(int64_t K, int64_t N, int G, int dtype) {
   return W4A16_OK;
 }
 
-// W4A16_FORCE_PATH=generic|decode|prefill restricts the dispatcher (tests and benchmarks only).
+// A path the dispatcher is restricted to (tests and benchmarks only): set by
+// w4a16_debug_force_path, initially from the environment variable W4A16_FORCE_PATH
+// (generic|decode|prefill), read once. -1: no restriction; -2: not read yet.
+std::atomic<int> g_forced_path{-2};
 int forced_path() {
+  int f = g_forced_path.load(std::memory_order_relaxed);
+  if (f != -2) return f;
   const char *s = std::getenv("W4A16_FORCE_PATH");
-  if (!s || !*s) return -1;
-  if (!std::strcmp(s, "generic")) return W4A16_PATH_GENERIC;
-  if (!std::strcmp(s, "decode")) return W4A16_PATH_DECODE;
-  if (!std::strcmp(s, "prefill")) return W4A16_PATH_PREFILL;
-  return -1;
+  int v = -1;
+  if (s && !std::strcmp(s, "generic")) v = W4A16_PATH_GENERIC;
+  else if (s && !std::strcmp(s, "decode")) v = W4A16_PATH_DECODE;
+  else if (s && !std::strcmp(s, "prefill")) v = W4A16_PATH_PREFILL;
+  int expected = -2;
+  g_forced_path.compare_exchange_strong(expected, v, std::memory_order_relaxed);
+  return g_forced_path.load(std::memory_order_relaxed);
 }
 
 // M at and above which the tcgen05 path is preferred when it applies.
@@ -127,7 +135,55 @@ void choose_plan(const GemmArgs &g, int num_sms, bool tma, bool query_device, bo
   }
 }
 
+// The dispatcher's choice depends on the shape, the dtype, whether zero points are given, which
+// pointers are 16-byte aligned, whether a workspace is offered, the forced path and the device.
+// Plans are kept per such key, so that a repeated shape costs one lookup on the host.
+struct PlanKey {
+  int64_t M, K, N;
+  int G, dtype, device, force;
+  uint32_t flags;
+  bool operator==(const PlanKey &o) const {
+    return M == o.M && K == o.K && N == o.N && G == o.G && dtype == o.dtype && device == o.device &&
+           force == o.force && flags == o.flags;
+  }
+};
+struct PlanKeyHash {
+  size_t operator()(const PlanKey &k) const {
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&](uint64_t v) { h = (h ^ v) * 1099511628211ull; };
+    mix(uint64_t(k.M)); mix(uint64_t(k.K)); mix(uint64_t(k.N)); mix(uint64_t(k.G));
+    mix(uint64_t(k.dtype) | (uint64_t(k.device) << 8) | (uint64_t(k.force + 8) << 24) | (uint64_t(k.flags) << 32));
+    return static_cast<size_t>(h);
+  }
+};
+
+uint32_t plan_flags(const GemmArgs &g, bool workspace, bool tma) {
+  auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  return (g.qzeros ? 1u : 0u) | (workspace ? 2u : 0u) | (tma ? 4u : 0u) | (a16(g.a) ? 8u : 0u) |
+         (a16(g.b_q) ? 16u : 0u) | (a16(g.scales) ? 32u : 0u) | (!g.qzeros || a16(g.qzeros) ? 64u : 0u) |
+         (a16(g.out) ? 128u : 0u) | (!g.bias || a16(g.bias) ? 256u : 0u);
+}
+
 }  // namespace
+
+void cached_plan(const GemmArgs &g, const DeviceInfo &dev, bool workspace, w4a16_plan_t *plan) {
+  static std::mutex mu;
+  static std::unordered_map<PlanKey, w4a16_plan_t, PlanKeyHash> plans;
+  const bool tma = tma_available();
+  const PlanKey key{g.M, g.K, g.N, g.group_size, g.dtype, dev.device, forced_path(), plan_flags(g, workspace, tma)};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = plans.find(key);
+    if (it != plans.end()) {
+      *plan = it->second;
+      return;
+    }
+  }
+  choose_plan(g, dev.num_sms, tma, /*query_device=*/true, workspace, plan);
+  std::lock_guard<std::mutex> lock(mu);
+  if (plans.size() >= 4096) plans.clear();  // bounded: a workload with ever-new shapes re-plans
+  plans.emplace(key, *plan);
+}
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
@@ -318,11 +374,9 @@ static w4a16_status gemm_impl(GemmArgs &g) {
   cudaError_t e = current_device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "device query");
   w4a16_plan_t plan;
-  const bool tma = tma_available();
-  choose_plan(g, dev.num_sms, tma, /*query_device=*/true, g.workspace != nullptr, &plan);
+  cached_plan(g, dev, g.workspace != nullptr, &plan);
   // a stream-K plan whose workspace the caller did not provide in full falls back to whole tiles
-  if (g.workspace && g.workspace_bytes < prefill_plan_workspace_bytes(plan))
-    choose_plan(g, dev.num_sms, tma, /*query_device=*/true, /*workspace=*/false, &plan);
+  if (g.workspace && g.workspace_bytes < prefill_plan_workspace_bytes(plan)) cached_plan(g, dev, false, &plan);
   switch (plan.path) {
     case W4A16_PATH_DECODE: e = launch_gemm_decode(g, plan); break;
     case W4A16_PATH_PREFILL: e = launch_gemm_prefill(g, plan); break;
@@ -377,7 +431,7 @@ w4a16_status w4a16_gemm_noalloc(const void *a, const int32_t *b_q, const void *s
   if (e != cudaSuccess) return cuda_fail(e, "static scratch address (cudaGetSymbolAddress)");
   // the plan this call will run (gemm_impl makes the same choice); only stream-K needs scratch
   w4a16_plan_t plan;
-  choose_plan(g, dev.num_sms, tma_available(), /*query_device=*/true, /*workspace=*/true, &plan);
+  cached_plan(g, dev, /*workspace=*/true, &plan);
   const size_t need = prefill_plan_workspace_bytes(plan);
   if (need > scratch_bytes)
     return fail(W4A16_ERR_UNSUPPORTED,
@@ -392,6 +446,123 @@ w4a16_status w4a16_gemm_noalloc(const void *a, const int32_t *b_q, const void *s
   g.workspace = scratch;
   g.workspace_bytes = scratch_bytes;
   return gemm_impl(g);
+}
+
+}  // extern "C"
+
+// A prepared layer: the weights' configuration checked once, the dispatcher's plan and the weight
+// descriptors kept per call shape, so that a call validates and encodes only the activations.
+struct w4a16_layer_st {
+  GemmArgs proto;  // weights, group size, zero points, bias, K, N, dtype
+  int device = 0;
+  struct Entry {
+    w4a16_plan_t plan;
+    WeightMaps maps;
+    bool have_maps;
+  };
+  std::mutex mu;
+  std::unordered_map<uint64_t, Entry> cache;  // key: M, plan flags, forced path
+};
+
+extern "C" {
+
+w4a16_status w4a16_layer_create(const int32_t *b_q, const void *scales, const int32_t *qzeros, int group_size,
+                                int zp_bias, const void *bias, int64_t k, int64_t n, w4a16_dtype dtype,
+                                w4a16_layer_t *layer) {
+  if (!layer) return fail(W4A16_ERR_INVALID_ARG, "layer must not be NULL");
+  *layer = nullptr;
+  w4a16_status st = check_config(k, n, group_size, dtype);
+  if (st != W4A16_OK) return st;
+  if (!qzeros && (zp_bias < 0 || zp_bias > 15))
+    return fail(W4A16_ERR_INVALID_ARG, "zp_bias (%d) must be in [0, 15]", zp_bias);
+  if (!b_q || !scales) return fail(W4A16_ERR_INVALID_ARG, "b_q and scales must not be NULL");
+  if (!aligned(b_q, 4) || !aligned(scales, 2) || (qzeros && !aligned(qzeros, 4)) || (bias && !aligned(bias, 2)))
+    return fail(W4A16_ERR_MISALIGNED, "tensors must be naturally aligned (2 bytes for 16-bit, 4 for int32)");
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  auto *L = new (std::nothrow) w4a16_layer_st;
+  if (!L) return fail(W4A16_ERR_INVALID_ARG, "out of host memory");
+  L->proto = GemmArgs{nullptr, b_q, scales, qzeros, group_size, zp_bias, bias, nullptr, 0, k, n,
+                      static_cast<int>(dtype), nullptr};
+  L->device = dev;
+  *layer = L;
+  return ok();
+}
+
+w4a16_status w4a16_layer_destroy(w4a16_layer_t layer) {
+  delete layer;
+  return ok();
+}
+
+size_t w4a16_layer_workspace_size(w4a16_layer_t layer, int64_t m) {
+  if (!layer) return 0;
+  return w4a16_gemm_workspace_size(m, layer->proto.K, layer->proto.N, layer->proto.group_size, layer->proto.dtype);
+}
+
+w4a16_status w4a16_layer_gemm(w4a16_layer_t layer, const void *a, void *out, int64_t m, void *workspace,
+                              size_t workspace_bytes, w4a16_stream_t stream) {
+  if (!layer) return fail(W4A16_ERR_INVALID_ARG, "layer must not be NULL");
+  GemmArgs g = layer->proto;
+  g.a = a;
+  g.out = out;
+  g.M = m;
+  g.stream = reinterpret_cast<cudaStream_t>(stream);
+  g.workspace = workspace;
+  g.workspace_bytes = workspace ? workspace_bytes : 0;
+  if (m < 0 || m >= kMaxDim) return fail(W4A16_ERR_INVALID_ARG, "M (%lld) must be in [0, 2^31)", (long long)m);
+  if (m == 0) return ok();
+  if (!a || !out) return fail(W4A16_ERR_INVALID_ARG, "a and out must not be NULL");
+  if (!aligned(a, 2) || !aligned(out, 2)) return fail(W4A16_ERR_MISALIGNED, "a and out must be 2-byte aligned");
+  if (workspace && !aligned(workspace, 256)) return fail(W4A16_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+  const int64_t ng = g.K / g.group_size;
+  const Range o = range(out, m * g.N * 2);
+  if (overlaps(o, range(a, m * g.K * 2)) || overlaps(o, range(g.b_q, g.K * g.N / 2)) ||
+      overlaps(o, range(g.scales, ng * g.N * 2)) || (g.qzeros && overlaps(o, range(g.qzeros, ng * g.N / 2))) ||
+      (g.bias && overlaps(o, range(g.bias, g.N * 2))))
+    return fail(W4A16_ERR_INVALID_ARG, "out overlaps an input tensor");
+  if (workspace) {
+    const Range w = range(workspace, static_cast<int64_t>(workspace_bytes));
+    if (overlaps(w, o) || overlaps(w, range(a, m * g.K * 2)) || overlaps(w, range(g.b_q, g.K * g.N / 2)) ||
+        overlaps(w, range(g.scales, ng * g.N * 2)) || (g.qzeros && overlaps(w, range(g.qzeros, ng * g.N / 2))) ||
+        (g.bias && overlaps(w, range(g.bias, g.N * 2))))
+      return fail(W4A16_ERR_INVALID_ARG, "workspace overlaps a tensor argument");
+  }
+  DeviceInfo dev;
+  cudaError_t e = current_device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  if (dev.device != layer->device)
+    return fail(W4A16_ERR_INVALID_ARG, "the layer was prepared on device %d, the current device is %d", layer->device,
+                dev.device);
+  const bool tma = tma_available();
+  const int force = forced_path();
+  auto entry_for = [&](bool ws) -> w4a16_layer_st::Entry {
+    const uint64_t key = (uint64_t(m) << 20) | (uint64_t(plan_flags(g, ws, tma)) << 4) | uint64_t(force + 2);
+    {
+      std::lock_guard<std::mutex> lock(layer->mu);
+      auto it = layer->cache.find(key);
+      if (it != layer->cache.end()) return it->second;
+    }
+    w4a16_layer_st::Entry en{};
+    cached_plan(g, dev, ws, &en.plan);
+    if (en.plan.path == W4A16_PATH_DECODE) en.have_maps = decode_weight_maps(g, en.plan, &en.maps);
+    else if (en.plan.path == W4A16_PATH_PREFILL) en.have_maps = prefill_weight_maps(g, &en.maps);
+    std::lock_guard<std::mutex> lock(layer->mu);
+    if (layer->cache.size() >= 1024) layer->cache.clear();
+    layer->cache.emplace(key, en);
+    return en;
+  };
+  w4a16_layer_st::Entry en = entry_for(workspace != nullptr);
+  // a stream-K plan whose workspace the caller did not provide in full falls back to whole tiles
+  if (workspace && workspace_bytes < prefill_plan_workspace_bytes(en.plan)) en = entry_for(false);
+  const WeightMaps *wm = en.have_maps ? &en.maps : nullptr;
+  switch (en.plan.path) {
+    case W4A16_PATH_DECODE: e = launch_gemm_decode(g, en.plan, wm); break;
+    case W4A16_PATH_PREFILL: e = launch_gemm_prefill(g, en.plan, wm); break;
+    default: e = launch_gemm_generic(g); break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "w4a16_layer_gemm launch");
+  return ok();
 }
 
 size_t w4a16_gemm_workspace_size(int64_t m, int64_t k, int64_t n, int group_size, int dtype) {
@@ -447,6 +618,13 @@ w4a16_status w4a16_get_device_error(void) {
   if (e != cudaSuccess) return cuda_fail(e, "read device error word");
   err |= err2;
   if (err) return fail(W4A16_ERR_TIMEOUT, "a bounded device-side wait gave up (code 0x%x)", err);
+  return ok();
+}
+
+w4a16_status w4a16_debug_force_path(int path) {
+  if (path != -1 && path != W4A16_PATH_GENERIC && path != W4A16_PATH_DECODE && path != W4A16_PATH_PREFILL)
+    return fail(W4A16_ERR_INVALID_ARG, "path %d is not -1, W4A16_PATH_GENERIC, _DECODE or _PREFILL", path);
+  g_forced_path.store(path, std::memory_order_relaxed);
   return ok();
 }
 

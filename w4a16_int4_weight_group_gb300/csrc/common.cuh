@@ -159,6 +159,18 @@ __device__ __forceinline__ void cluster_sync_all() {
 __device__ __forceinline__ void cluster_sync_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
+// Split phases of the cluster barrier: arrive (no memory ordering) now, wait later.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// Asynchronous 4-byte store into the shared memory of a CTA of the cluster (shared::cluster address),
+// completion counted in bytes on that CTA's mbarrier (shared::cluster address).
+__device__ __forceinline__ void st_async_f32(uint32_t cluster_addr, float v, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cluster_addr),
+               "r"(__float_as_uint(v)), "r"(cluster_bar)
+               : "memory");
+}
 // Maps a shared::cta address of this CTA to the same offset in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
   uint32_t r;
@@ -231,6 +243,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tensor_map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
+}
+// Asks the memory system to bring a 2-D tile of a tensor into L2 (no shared-memory destination, no
+// completion to wait for): a hint that lets a kernel start HBM reads before it may consume them.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void *tensor_map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tensor_map)),
+               "r"(c0), "r"(c1)
+               : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // Orders this thread's earlier generic-proxy view of global memory (e.g. after an acquire of data

@@ -44,18 +44,33 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kBlocksPerRow = 8;               // 32-column blocks of a 256-column tile
-constexpr int kGroups = 2;                     // consumer groups taking alternate K blocks
-constexpr int kConsumers = kBlocksPerRow * kGroups;
-constexpr int kThreads = 32 * (kConsumers + 1);
+constexpr int kBlocksPerRow = 8;               // 32-column blocks of a 256-column tile: consumer warps per group
 constexpr int BN = 256;                        // output columns per CTA
 constexpr int BK = 64;                         // rows of K per block
-constexpr int kRingBlocks = 16;                // K blocks the ring holds (stages x blocks per stage)
-constexpr int kMaxStages = kRingBlocks;        // with one block per stage
+// K blocks the ring holds, per consumer-group count. One group: an 8-block ring keeps the CTA under
+// half of the SM's shared memory, so a CTA of the next call can be resident beside it and fetch its
+// weights before this call ends. Two groups: a 16-block ring, one CTA per SM.
+#ifndef W4A16_DEC_RING1
+#define W4A16_DEC_RING1 8
+#endif
+#ifndef W4A16_DEC_RING2
+#define W4A16_DEC_RING2 16
+#endif
+// Zero-point handling on the tensor core: 0 = subtract (base + zp) from every weight pair before the
+// MMA; 1 = multiply the magic values (base + q) and remove (base + zp) * rowsum(A) per group in fp32;
+// 2 = the latter only when a K block holds one scale group. Up to 8 rows of A only (the row sums of
+// a 16-row batch would not fit the registers).
+#ifndef W4A16_DEC_RS
+#define W4A16_DEC_RS 2
+#endif
+#ifndef W4A16_DEC_MINB2
+#define W4A16_DEC_MINB2 1
+#endif
+__host__ __device__ constexpr int ring_blocks(int ncg) { return ncg == 1 ? W4A16_DEC_RING1 : W4A16_DEC_RING2; }
+__host__ __device__ constexpr int threads_of(int ncg) { return 32 * (kBlocksPerRow * ncg + 1); }
 // K blocks whose copies a CTA keeps in flight. A stage is requested once the stage this many blocks
 // earlier has landed (and its ring slot is free): measured on GB300, 8 blocks (64 KB) per SM move a
-// 25 MB layer 10 % faster than requesting the whole 16-block ring at once (the first blocks of
-// every CTA land sooner when the memory system holds fewer requests), and 4-6 blocks are slower.
+// 25 MB layer 10 % faster than requesting a 16-block ring at once, and 4-6 blocks are slower.
 constexpr int kInFlightBlocks = 8;
 constexpr int kMaxCluster = 16;  // split-K factor: cluster sizes above 8 are non-portable
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
@@ -64,24 +79,30 @@ __device__ unsigned int g_decode_error;
 __device__ unsigned long long g_decode_wait_limit_ns;
 __device__ unsigned int g_decode_stall;  // test hook: consumers first wait on a barrier nobody arrives on
 
-template <int J>
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+template <int J, int NCG>
 struct Layout {
+  static constexpr int R = ring_blocks(NCG);    // ring depth in K blocks (a power of two)
   static constexpr int kP = BK * BN / 2;        // 8 KB packed weights per K block
   static constexpr int kA = 8 * J * BK * 2;     // 1 KB per 8 rows of A per K block
   static constexpr int kS = 2 * BN * 2;         // two scale rows per K block slot
   static constexpr int kZ = 2 * (BN / 8) * 4;   // two zero-point rows per K block slot
   static constexpr int kOffP = 0;
-  static constexpr int kOffA = kOffP + kRingBlocks * kP;
-  static constexpr int kOffS = kOffA + kRingBlocks * kA;
-  static constexpr int kOffZ = kOffS + kRingBlocks * kS;
-  static constexpr int kOffBar = kOffZ + kRingBlocks * kZ;
-  // full[kMaxStages], empty[kMaxStages], the stall-test barrier
-  static constexpr int kOffFlag = kOffBar + (2 * kMaxStages + 1) * 8;
-  static constexpr int kOffRed = kOffFlag + 16;                       // split-K partial tile [8J][256]
-  static constexpr int kOffGRed = kOffRed + 8 * J * BN * 4;           // second group's partial tile
-  static constexpr int kGRedBytes = 8 * J * BN * 4;
-  static constexpr int kUsed = kOffGRed + kGRedBytes;
+  static constexpr int kOffA = kOffP + R * kP;
+  static constexpr int kOffS = kOffA + R * kA;
+  static constexpr int kOffZ = kOffS + R * kS;
+  // Split-K receive buffer: this CTA's slice of the tile's live outputs from every (rank, consumer
+  // group), fp32, written by the other CTAs of the cluster (and by this one) with st.async. At most
+  // NCG x (8J x 256 + 16) floats: C slices of ceil(live / C) elements per contributor group.
+  static constexpr int kRecvFloats = NCG * (8 * J * BN + kMaxCluster);
+  static constexpr int kOffRecv = kOffZ + R * kZ;
+  static constexpr int kOffBar = kOffRecv + kRecvFloats * 4;
+  // full[R], empty[R], the stall-test barrier, the receive barrier
+  static constexpr int kOffFlag = kOffBar + (2 * R + 2) * 8;
+  static constexpr int kUsed = kOffFlag + 16;
   static constexpr int kSmem = kUsed + 1024;    // slack to align the base to 1024 bytes
+  static_assert((R & (R - 1)) == 0 && R >= 4, "ring depth: a power of two");
   static_assert(kOffA % 1024 == 0 && kA % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
 
@@ -96,6 +117,7 @@ struct DecodeParams {
   int kb_total;     // K blocks of the problem
   int srows;        // scale / zero-point rows per stage
   int g_shift;      // log2(G) when a stage spans several scale groups, else 31 (one group per stage)
+  int bpg;          // K blocks per scale group for G in {64, 128}; 0 when a group outlasts every stage
 };
 
 // A 16-bit float (fp16 or bf16 bits) widened exactly to fp32.
@@ -106,7 +128,8 @@ __device__ __forceinline__ float bits_to_f32(uint32_t h) {
 }
 
 // Packed (base + q) pairs of the four columns of a quad from one ldmatrix.trans register
-// (low half: row k, high half: row k+1, four nibbles each).
+// (low half: row k, high half: row k+1, four nibbles each). base is 1024 for fp16 columns 0 and 2
+// (low nibble of a byte), 64 for fp16 columns 1 and 3 (high nibble), 128 for bf16.
 template <bool BF>
 __device__ __forceinline__ void magic_quad(uint32_t w, uint32_t (&h)[4]) {
   if constexpr (BF) {
@@ -122,15 +145,23 @@ __device__ __forceinline__ void magic_quad(uint32_t w, uint32_t (&h)[4]) {
     h[3] = and_or(w8, 0x00F000F0u, 0x54005400u);
   }
 }
+template <bool BF>
+__host__ __device__ constexpr float magic_base(int j) {
+  return BF ? 128.f : ((j & 1) ? 64.f : 1024.f);
+}
 
-template <class DT, int J, bool HAS_ZP, bool TWO_GROUPS, int SBS>
-__global__ void __launch_bounds__(kThreads, 1)
+template <class DT, int J, bool HAS_ZP, bool TWO_GROUPS, int SBS, int NCG>
+__global__ void __launch_bounds__(threads_of(NCG), NCG == 1 ? 2 : W4A16_DEC_MINB2)
     decode_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmP,
                   const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ,
                   const DecodeParams p) {
-  using L = Layout<J>;
+  using L = Layout<J, NCG>;
   using T = typename DT::T;
   constexpr bool BF = DT::kBF16;
+  constexpr int kConsumers = kBlocksPerRow * NCG;
+  constexpr int kThreads = threads_of(NCG);
+  // row-sum correction instead of per-pair subtraction (see W4A16_DEC_RS)
+  constexpr bool RS = J == 1 && (W4A16_DEC_RS == 1 || (W4A16_DEC_RS == 2 && !TWO_GROUPS));
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -145,29 +176,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t n0 = int64_t(blockIdx.x / C) * BN;
   const int kb_begin = min(p.kb_total, rank * p.kb_per_cta);
   const int nkb = min(p.kb_total, kb_begin + p.kb_per_cta) - kb_begin;
-  // K blocks per stage (1, 2 or 4) and stages in the ring, both compile-time (runtime shifts here
-  // cost more than the whole per-block index arithmetic they replace)
+  // K blocks per stage (1 or 4) and stages in the ring, both compile-time (runtime shifts here cost
+  // more than the whole per-block index arithmetic they replace)
   constexpr int sbs = SBS, SB = 1 << SBS;
-  constexpr int nsts = 4 - SBS, nst = 1 << nsts;
+  constexpr int nsts = ilog2(L::R) - SBS, nst = 1 << nsts;
   const int nss = (nkb + SB - 1) >> sbs;        // stages this CTA fills
 
-  const uint32_t full0 = base + L::kOffBar, empty0 = full0 + 8u * kMaxStages;
-  const uint32_t stall_bar = empty0 + 8u * kMaxStages;
+  const uint32_t full0 = base + L::kOffBar, empty0 = full0 + 8u * L::R;
+  const uint32_t stall_bar = empty0 + 8u * L::R;
+  const uint32_t recv_bar = stall_bar + 8u;
+  // Split-K exchange: the live outputs (rows below M) of the tile, flattened o = m * 256 + n, are cut
+  // into C slices of `per` elements; rank s adds slice s over every (rank, group) contribution.
+  const int64_t rows = p.M < 8 * J ? p.M : 8 * J;
+  const bool push = C > 1 || NCG > 1;
+  const int live = static_cast<int>(rows) * BN;
+  const int per = (live + C - 1) / C;
+  const int my_per = max(0, min(per, live - rank * per));
   const uint32_t abort_flag = base + L::kOffFlag;
   const unsigned long long lim = g_decode_wait_limit_ns;
   const uint64_t limit_ns = lim ? lim : kDefaultWaitNs;
 
   if (threadIdx.x == 0) {
-    // a stage is released by every consumer warp that reads a block of it: one group when a stage
-    // holds one block (the groups alternate stages), both groups otherwise
-    const uint32_t readers = SB == 1 ? kBlocksPerRow : kConsumers;
+    // a stage is released by the eight consumer warps of the group that reads it (the groups take
+    // alternate stages)
+    const uint32_t readers = kBlocksPerRow;
     for (int s = 0; s < nst; ++s) {
       mbar_init(full0 + 8u * s, 1);
       mbar_init(empty0 + 8u * s, readers);
     }
     mbar_init(stall_bar, 1);
+    mbar_init(recv_bar, 1);
     st_flag(abort_flag, 0u);
     mbar_init_fence();
+    // every contribution to this CTA's slice lands with st.async, counted in bytes on recv_bar
+    if (push) mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(C * NCG * my_per * 4));
   }
   if (warp == kConsumers && lane == 0) {
     // descriptors live in the kernel parameters, not in memory an earlier kernel writes
@@ -177,6 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (HAS_ZP) prefetch_tensormap(&tmZ);
   }
   __syncthreads();
+  // the peers' receive barriers are initialised before any CTA of the cluster pushes to them (this
+  // runs before the dependency wait, so it overlaps the previous kernel)
+  if (C > 1) cluster_sync_all();
   // Let the next kernel of the stream begin launching (it waits for this one before touching its
   // own inputs). Everything this kernel reads except the weights may come from the previous kernel.
   griddep_launch_dependents();
@@ -247,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------------ consumers
     griddep_wait();  // the epilogue writes `out` and reads `bias`: the previous kernel must be done
-    const int grp = warp / kBlocksPerRow;  // K blocks grp, grp+2, grp+4, ...
+    const int grp = warp / kBlocksPerRow;  // stages grp, grp+NCG, grp+2*NCG, ...
     const int cb = warp % kBlocksPerRow;   // 16-byte chunk (32 columns) of every 128-byte packed row
     // ldmatrix row addresses: lanes 8i..8i+7 -> matrix i, row (lane & 7)
     const int mi = lane >> 3, rj = lane & 7;
@@ -257,165 +302,186 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_off = uint32_t((32 * cb + 4 * gl) * 2);
     const uint32_t z_off = uint32_t((4 * cb + (gl >> 1)) * 4);
     const int z_shift = 16 * (gl & 1);
-    constexpr int kSRows = TWO_GROUPS ? 2 : 1;  // scale groups per K block
+    constexpr int kSeg = TWO_GROUPS ? 2 : 1;  // scale-group segments per K block (32 rows each for G = 32)
+    const bool single_row = p.M == 1;         // only accumulator column m = 0 is live
 
-    // Column j of this lane's quad (output column n0 + 32 cb + 4 gl + j) holds magic values base_j + q:
-    // fp16 uses 1024 for even j (low nibble of a byte) and 64 for odd j (high nibble), bf16 uses 128.
-    // zsub[j] = (base_j + zp, base_j + zp) in the activation dtype: the same unpack applied to a word
-    // whose four nibbles are the zero points, in both halves. sc[j] = scale (fp32).
+    // Column j of this lane's quad (output column n0 + 32 cb + 4 gl + j) holds magic values base_j + q
+    // (magic_quad). Subtracting form: zsym[j] = (base_j + zp, base_j + zp) in the activation dtype,
+    // the same unpack applied to a word whose four nibbles are the zero point. Row-sum form:
+    // nzsym[j] = -(base_j + zp) in fp32.
     uint32_t zsym[4];
-    float sc[4];
-    if constexpr (!HAS_ZP) magic_quad<BF>(static_cast<uint32_t>(p.zp_bias) * 0x11111111u, zsym);
+    float nzsym[4];
+    if constexpr (!HAS_ZP) {
+      magic_quad<BF>(static_cast<uint32_t>(p.zp_bias) * 0x11111111u, zsym);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) nzsym[j] = -(magic_base<BF>(j) + static_cast<float>(p.zp_bias));
+    }
+    // a 16 x 16 operand of ones: its product with a block of activations is the block's row sums
+    constexpr uint32_t kOnes = BF ? 0x3F803F80u : 0x3C003C00u;
+    const uint32_t ones[4] = {kOnes, kOnes, kOnes, kOnes};
     bool ok = true;
     if (g_decode_stall) {  // failure-detection test: a wait that can only run out
       ok = wait_phase(stall_bar, 0, abort_flag, limit_ns, &g_decode_error);
       ok = __all_sync(0xffffffffu, ok);
     }
-    // Fragments of one K block: packed weights (row blocks 0..7 of column block cb), activation
-    // fragments (b0, b1 for k16 steps 0..3), raw scale and zero-point words of its group(s).
-    struct Frag {
-      uint32_t wq[8];
-      uint32_t af[J][8];
-      uint32_t sraw[kSRows][2];
-      uint32_t zraw[kSRows];
-    };
-    // Waits for K block i and loads its fragments; after this group's last block of the stage the
-    // stage is released (every value needed from it is in registers).
-    auto fetch = [&](int i, Frag &f) -> bool {
-      const int js = i >> sbs, b = i & (SB - 1);  // stage sequence number and block within the stage
-      const int s = js & (nst - 1);
-      bool w = wait_phase(full0 + 8u * s, (js >> nsts) & 1, abort_flag, limit_ns, &g_decode_error);
-      w = __all_sync(0xffffffffu, w);
-      if (!w) return false;
-      const uint32_t P = base + L::kOffP + (s * SB + b) * L::kP;
-      const uint32_t A = base + L::kOffA + (s * SB + b) * L::kA;
-      // scale and zero-point rows of this block's group(s) within the stage's rows
-      const int r0 = (b * BK) >> p.g_shift;
-      const uint32_t S = base + L::kOffS + s * SB * L::kS + r0 * (BN * 2);
-      const uint32_t Z = base + L::kOffZ + s * SB * L::kZ + r0 * (BN / 2);
-      uint32_t r[4];
-      ldsm_x4_trans(P + p_off, r);
-      f.wq[0] = r[0]; f.wq[1] = r[1]; f.wq[2] = r[2]; f.wq[3] = r[3];
-      ldsm_x4_trans(P + p_off + 4096u, r);
-      f.wq[4] = r[0]; f.wq[5] = r[1]; f.wq[6] = r[2]; f.wq[7] = r[3];
-#pragma unroll
-      for (int jt = 0; jt < J; ++jt) {
-        ldsm_x4(A + jt * 1024u + a_off, r);
-        f.af[jt][0] = r[0]; f.af[jt][1] = r[1]; f.af[jt][2] = r[2]; f.af[jt][3] = r[3];
-        ldsm_x4(A + jt * 1024u + a_off2, r);
-        f.af[jt][4] = r[0]; f.af[jt][5] = r[1]; f.af[jt][6] = r[2]; f.af[jt][7] = r[3];
-      }
-#pragma unroll
-      for (int g = 0; g < kSRows; ++g) {
-        lds64(S + g * (BN * 2) + s_off, f.sraw[g][0], f.sraw[g][1]);
-        if constexpr (HAS_ZP) f.zraw[g] = lds32(Z + g * (BN / 2) + z_off) >> z_shift;
-      }
-      __syncwarp();
-      if (lane == 0 && (((i + kGroups) >> sbs) != js || i + kGroups >= nkb)) mbar_arrive(empty0 + 8u * s);
-      return true;
-    };
-    // Products on the tensor core for scale group g of a block: one packed subtraction per pair turns
-    // (base_j + q) into q - zp, exactly (a small integer), and blk = sum_k A[m,k] (q[k,n] - zp) over
-    // the group's k16 steps accumulates in fp32; then one fp32 multiply by the scale.
-    auto products = [&](const Frag &f, int g, float (&blk)[J][2][4]) {
+    // Partial products of the current scale group (fp32): blk = sum_k A[m,k] w[k,n] over the rows of
+    // the group seen so far, rs = sum_k A[m,k] (row-sum form). They are scaled into acc when the
+    // group ends, or when a stage ends inside it.
+    float blk[J][2][4], rs[J][4];
+    bool fresh = true;  // the next MMAs start blk and rs from zero
+    // Products of one segment (k16 steps t0 .. t0+kSteps-1 of a K block) on the tensor core.
+    // Subtracting form: one packed subtraction per pair turns (base_j + q) into q - zp, exactly (a
+    // small integer). Row-sum form: the magic values go in as they are and the product with the ones
+    // operand gives the row sums for the correction.
+    auto products = [&](const uint32_t (&wq)[8], const uint32_t (&af)[J][8], int seg, uint32_t zraw) {
       constexpr int kSteps = TWO_GROUPS ? 2 : 4;
       uint32_t zsub[4];
-      if constexpr (HAS_ZP) {
-        magic_quad<BF>(prmt(f.zraw[g], 0u, 0x1010u), zsub);  // this quad's zero points in both halves
-      } else {
+      if constexpr (!RS) {
+        if constexpr (HAS_ZP) {
+          magic_quad<BF>(prmt(zraw, 0u, 0x1010u), zsub);  // this quad's zero points in both halves
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) zsub[j] = zsym[j];
+          for (int j = 0; j < 4; ++j) zsub[j] = zsym[j];
+        }
       }
 #pragma unroll
       for (int tt = 0; tt < kSteps; ++tt) {
-        const int t = g * kSteps + tt;
+        const int t = seg * kSteps + tt;
         uint32_t lo[4], hi[4];
-        magic_quad<BF>(f.wq[2 * t], lo);
-        magic_quad<BF>(f.wq[2 * t + 1], hi);
+        magic_quad<BF>(wq[2 * t], lo);
+        magic_quad<BF>(wq[2 * t + 1], hi);
+        if constexpr (!RS) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          lo[j] = sub2_rn<BF>(lo[j], zsub[j]);
-          hi[j] = sub2_rn<BF>(hi[j], zsub[j]);
+          for (int j = 0; j < 4; ++j) {
+            lo[j] = sub2_rn<BF>(lo[j], zsub[j]);
+            hi[j] = sub2_rn<BF>(hi[j], zsub[j]);
+          }
         }
         // MMA rows: g -> column 4*gl + j, g + 8 -> column 4*gl + j + 2, for j = 0 and j = 1
         const uint32_t a0[4] = {lo[0], lo[2], hi[0], hi[2]};
         const uint32_t a1[4] = {lo[1], lo[3], hi[1], hi[3]};
 #pragma unroll
         for (int jt = 0; jt < J; ++jt) {
-          if (tt == 0) {
-            mma_16816_z<BF>(blk[jt][0], a0, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
-            mma_16816_z<BF>(blk[jt][1], a1, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
+          if (fresh && tt == 0) {
+            mma_16816_z<BF>(blk[jt][0], a0, af[jt][2 * t], af[jt][2 * t + 1]);
+            mma_16816_z<BF>(blk[jt][1], a1, af[jt][2 * t], af[jt][2 * t + 1]);
+            if constexpr (RS) mma_16816_z<BF>(rs[jt], ones, af[jt][2 * t], af[jt][2 * t + 1]);
           } else {
-            mma_16816<BF>(blk[jt][0], a0, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
-            mma_16816<BF>(blk[jt][1], a1, f.af[jt][2 * t], f.af[jt][2 * t + 1]);
+            mma_16816<BF>(blk[jt][0], a0, af[jt][2 * t], af[jt][2 * t + 1]);
+            mma_16816<BF>(blk[jt][1], a1, af[jt][2 * t], af[jt][2 * t + 1]);
+            if constexpr (RS) mma_16816<BF>(rs[jt], ones, af[jt][2 * t], af[jt][2 * t + 1]);
           }
         }
       }
+      fresh = false;
     };
-    auto scale_add = [&](const Frag &f, int g, const float (&blk)[J][2][4]) {
+    // Ends a scale group: acc += s * blk (subtracting form) or acc += s * (blk - (base + zp) * rs)
+    // (row-sum form), in fp32. With one-hot activations both give exactly s * (q - zp): blk and rs
+    // are exact, and so are the fused multiply-adds on these small integers. With M = 1 only the
+    // accumulator elements of row 0 (the even ones) are updated.
+    auto flush = [&](const uint32_t (&sraw)[2], uint32_t zraw) {
+      float sc[4], nz[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint32_t h = (j < 2 ? f.sraw[g][0] : f.sraw[g][1]) >> (16 * (j & 1));
+        const uint32_t h = (j < 2 ? sraw[0] : sraw[1]) >> (16 * (j & 1));
         sc[j] = bits_to_f32<BF>(h & 0xFFFFu);
       }
+      if constexpr (RS) {
+        if constexpr (HAS_ZP) {
+          // -(base_j + zp_j): (2^23 - base_j) - (2^23 + zp_j), the second term built from the nibble
+          // as the bits of a float (exact: both are integers below 2^24)
 #pragma unroll
-      for (int jt = 0; jt < J; ++jt)
+          for (int j = 0; j < 4; ++j)
+            nz[j] = (8388608.f - magic_base<BF>(j)) - __uint_as_float(0x4B000000u | ((zraw >> (4 * j)) & 0xFu));
+        } else {
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+          for (int j = 0; j < 4; ++j) nz[j] = nzsym[j];
+        }
+      }
+      auto update = [&](int jt, int q, int e) {
+        const int j = q + 2 * (e >> 1);  // accumulator element e of MMA q holds column j
+        if constexpr (RS) {
+          const float tv = fmaf(nz[j], rs[jt][e & 1], blk[jt][q][e]);
+          acc[jt][q][e] = fmaf(sc[j], tv, acc[jt][q][e]);
+        } else {
+          acc[jt][q][e] = fmaf(sc[j], blk[jt][q][e], acc[jt][q][e]);
+        }
+      };
+      if (J == 1 && single_row) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = q + 2 * (e >> 1);  // accumulator element e of MMA q holds column j
-            acc[jt][q][e] = fmaf(sc[j], blk[jt][q][e], acc[jt][q][e]);
-          }
+        for (int q = 0; q < 2; ++q) {
+          update(0, q, 0);
+          update(0, q, 2);
+        }
+      } else {
+#pragma unroll
+        for (int jt = 0; jt < J; ++jt)
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) update(jt, q, e);
+      }
+      fresh = true;
     };
-    Frag f;
-    for (int i = grp; i < nkb && ok; i += kGroups) {
-      ok = fetch(i, f);
+    // The group's stages, one at a time: wait for the stage, then per K block load the fragments
+    // (packed weights by ldmatrix.trans, activations by ldmatrix, the block's scale and zero-point
+    // words), release the stage after the last block's loads, and multiply; a scale group ends after
+    // the block whose end is a multiple of G (or the stage's last block, or each 32-row half for
+    // G = 32).
+    for (int js = grp; js < nss && ok; js += NCG) {
+      const int s = js & (nst - 1);
+      ok = wait_phase(full0 + 8u * s, (js >> nsts) & 1, abort_flag, limit_ns, &g_decode_error);
+      ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
+      const int nb = min(SB, nkb - js * SB);
+      const uint32_t P0 = base + L::kOffP + s * SB * L::kP;
+      const uint32_t A0 = base + L::kOffA + s * SB * L::kA;
+      const uint32_t S0 = base + L::kOffS + s * SB * L::kS + s_off;
+      const uint32_t Z0 = base + L::kOffZ + s * SB * L::kZ + z_off;
 #pragma unroll
-      for (int g = 0; g < kSRows; ++g) {
-        float blk[J][2][4];
-        products(f, g, blk);
-        scale_add(f, g, blk);
+      for (int b = 0; b < SB; ++b) {
+        if (b < nb) {
+          uint32_t wq[8], af[J][8], r[4];
+          const uint32_t P = P0 + b * L::kP;
+          ldsm_x4_trans(P + p_off, r);
+          wq[0] = r[0]; wq[1] = r[1]; wq[2] = r[2]; wq[3] = r[3];
+          ldsm_x4_trans(P + p_off + 4096u, r);
+          wq[4] = r[0]; wq[5] = r[1]; wq[6] = r[2]; wq[7] = r[3];
+#pragma unroll
+          for (int jt = 0; jt < J; ++jt) {
+            const uint32_t A = A0 + b * L::kA + jt * 1024u;
+            ldsm_x4(A + a_off, r);
+            af[jt][0] = r[0]; af[jt][1] = r[1]; af[jt][2] = r[2]; af[jt][3] = r[3];
+            ldsm_x4(A + a_off2, r);
+            af[jt][4] = r[0]; af[jt][5] = r[1]; af[jt][6] = r[2]; af[jt][7] = r[3];
+          }
+          // scale and zero-point rows of this block's group(s) within the stage's rows
+          uint32_t sraw[kSeg][2], zraw[kSeg];
+          const int r0 = (b * BK) >> p.g_shift;
+#pragma unroll
+          for (int g = 0; g < kSeg; ++g) {
+            lds64(S0 + (r0 + g) * (BN * 2), sraw[g][0], sraw[g][1]);
+            zraw[g] = HAS_ZP ? (lds32(Z0 + (r0 + g) * (BN / 2)) >> z_shift) : 0u;
+          }
+          if (b == nb - 1) {  // every value this group needs from the stage is in registers
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8u * s);
+          }
+#pragma unroll
+          for (int g = 0; g < kSeg; ++g) {
+            products(wq, af, g, zraw[g]);
+            // end of a scale group: every segment for G = 32; for larger G the block whose end is
+            // a multiple of G; and always the stage's last block
+            const int kend = kb_begin + js * SB + b + 1;  // K blocks done after this one
+            if (TWO_GROUPS || b == nb - 1 || (p.bpg > 0 && kend % p.bpg == 0)) flush(sraw[g], zraw[g]);
+          }
+        }
       }
     }
   }
 
   // ------------------------------------------------------------------ reduction and epilogue
-  __syncwarp();  // the producer warp's lanes meet again before the warp-aligned barriers below
-  // group 1 hands its partial sums to group 0 (fixed order: group 0 + group 1)
-  {
-    float *gred = reinterpret_cast<float *>(base_ptr + L::kOffGRed);
-    const int nl = 32 * (warp % kBlocksPerRow) + 4 * gl;
-    if (warp >= kBlocksPerRow && warp < kConsumers) {
-#pragma unroll
-      for (int jt = 0; jt < J; ++jt)
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int m = 8 * jt + 2 * tig;
-          gred[m * BN + nl + q] = acc[jt][q][0];
-          gred[(m + 1) * BN + nl + q] = acc[jt][q][1];
-          gred[m * BN + nl + q + 2] = acc[jt][q][2];
-          gred[(m + 1) * BN + nl + q + 2] = acc[jt][q][3];
-        }
-    }
-    // named barrier of the 16 consumer warps: the producer warp must not arrive on it (a 17th warp
-    // would open a second phase of the barrier that nobody completes)
-    if (warp < kConsumers) asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
-    if (warp < kBlocksPerRow) {
-#pragma unroll
-      for (int jt = 0; jt < J; ++jt)
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int m = 8 * jt + 2 * tig;
-          acc[jt][q][0] += gred[m * BN + nl + q];
-          acc[jt][q][1] += gred[(m + 1) * BN + nl + q];
-          acc[jt][q][2] += gred[m * BN + nl + q + 2];
-          acc[jt][q][3] += gred[(m + 1) * BN + nl + q + 2];
-        }
-    }
-  }
-  const int64_t rows = p.M < 8 * J ? p.M : 8 * J;
+  __syncwarp();  // the producer warp's lanes meet again before the cluster barrier below
   auto finish = [&](int m, int64_t n, float v) {
     if (m < rows && n < p.N) {
       if (p.bias) v += bits_to_float(p.bias[n], BF);
@@ -423,9 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       p.out[m * p.N + n] = *reinterpret_cast<const uint16_t *>(&y);
     }
   };
-  if (C == 1) {
+  const int nl0 = 32 * (warp % kBlocksPerRow) + 4 * gl;
+  if (!push) {
     if (warp < kBlocksPerRow) {
-      const int64_t nb = n0 + 32 * warp + 4 * gl;
+      const int64_t nb = n0 + nl0;
 #pragma unroll
       for (int jt = 0; jt < J; ++jt)
 #pragma unroll
@@ -438,44 +505,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
   } else {
-    // Split-K across the cluster: each rank publishes its partial tile in its own shared memory; after
-    // a cluster barrier, rank r reads slice r of every rank's tile (remote loads issued together,
-    // summed in rank order: deterministic); a second barrier keeps the tiles alive until all are read.
-    float *red = reinterpret_cast<float *>(base_ptr + L::kOffRed);
-    if (warp < kBlocksPerRow) {
-      const int nl = 32 * warp + 4 * gl;
+    // Split-K (cluster ranks and consumer groups): every consumer pushes each of its live partial
+    // sums into the receive buffer of the rank that adds that output, at the slot of its (rank,
+    // group); no cluster barrier and no remote load sits between the last product and the sums.
+    // A CTA that gave up a wait pushes nothing (its peers' receive waits then run out as well).
+    const bool aborted = ld_flag(abort_flag) != 0u;
+    if (warp < kConsumers && !aborted) {
+      const int slot = rank * NCG + warp / kBlocksPerRow;
+      const uint32_t recv0 = base + L::kOffRecv;
 #pragma unroll
       for (int jt = 0; jt < J; ++jt)
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int m = 8 * jt + 2 * tig;
-          red[m * BN + nl + q] = acc[jt][q][0];
-          red[(m + 1) * BN + nl + q] = acc[jt][q][1];
-          red[m * BN + nl + q + 2] = acc[jt][q][2];
-          red[(m + 1) * BN + nl + q + 2] = acc[jt][q][3];
-        }
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int m = 8 * jt + 2 * tig + (e & 1);
+            if (m < rows) {
+              const int o = m * BN + nl0 + q + 2 * (e >> 1);
+              const int dst = o / per;
+              const uint32_t a = recv0 + 4u * uint32_t(slot * per + (o - dst * per));
+              st_async_f32(map_to_rank(a, dst), acc[jt][q][e], map_to_rank(recv_bar, dst));
+            }
+          }
     }
-    cluster_sync_all();  // every rank's partial tile is complete and visible cluster-wide
-    constexpr int kTile = 8 * J * BN;
-    const int per = (kTile + C - 1) / C;
-    const int o_begin = rank * per;
-    const int o_end = o_begin + per < kTile ? o_begin + per : kTile;
-    const uint32_t red_u32 = base + L::kOffRed;
-    for (int o = o_begin + threadIdx.x; o < o_end; o += kThreads) {
-      const int m = o / BN;
-      if (m < rows) {
-        // issue every rank's load before summing (in rank order: deterministic)
-        float part[kMaxCluster];
-#pragma unroll
-        for (int rr = 0; rr < kMaxCluster; ++rr)
-          part[rr] = rr < C ? ld_dsmem_f32(map_to_rank(red_u32 + 4u * o, rr)) : 0.f;
+    if (C > 1) cluster_arrive_relaxed();
+    // this CTA's slice: wait for every contribution, add them in (rank, group) order, store
+    bool got = my_per == 0 || wait_phase(recv_bar, 0, abort_flag, limit_ns, &g_decode_error);
+    if (got) {
+      const float *recv = reinterpret_cast<const float *>(base_ptr + L::kOffRecv);
+      for (int i = threadIdx.x; i < my_per; i += kThreads) {
         float v = 0.f;
-#pragma unroll
-        for (int rr = 0; rr < kMaxCluster; ++rr) v += part[rr];
-        finish(m, n0 + (o % BN), v);
+        for (int sl = 0; sl < C * NCG; ++sl) v += recv[sl * per + i];
+        const int o = rank * per + i;
+        finish(o / BN, n0 + (o % BN), v);
       }
     }
-    cluster_sync_relaxed();  // keep this CTA's shared memory alive until every rank has read it
+    // no CTA leaves while a peer may still push into its receive buffer
+    if (C > 1) cluster_wait();
   }
 }
 
@@ -485,23 +551,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                           const DecodeParams);
 
-template <class DT, int J, int SBS>
+template <class DT, int J, int SBS, int NCG>
 KernelFn pick_zg(bool zp, bool two) {
-  if (zp) return two ? decode_kernel<DT, J, true, true, SBS> : decode_kernel<DT, J, true, false, SBS>;
-  return two ? decode_kernel<DT, J, false, true, SBS> : decode_kernel<DT, J, false, false, SBS>;
+  if (zp) return two ? decode_kernel<DT, J, true, true, SBS, NCG> : decode_kernel<DT, J, true, false, SBS, NCG>;
+  return two ? decode_kernel<DT, J, false, true, SBS, NCG> : decode_kernel<DT, J, false, false, SBS, NCG>;
 }
-template <class DT, int SBS>
+template <class DT, int SBS, int NCG>
 KernelFn pick_j(int J, bool zp, bool two) {
-  return J == 1 ? pick_zg<DT, 1, SBS>(zp, two) : pick_zg<DT, 2, SBS>(zp, two);
+  return J == 1 ? pick_zg<DT, 1, SBS, NCG>(zp, two) : pick_zg<DT, 2, SBS, NCG>(zp, two);
+}
+template <class DT, int NCG>
+KernelFn pick_sb(int J, bool zp, bool two, int sb) {
+  if (sb == 4) return pick_j<DT, 2, NCG>(J, zp, two);
+  return sb == 2 ? pick_j<DT, 1, NCG>(J, zp, two) : pick_j<DT, 0, NCG>(J, zp, two);
 }
 template <class DT>
-KernelFn pick_dt(int J, bool zp, bool two, int sb) {
-  if (sb == 4) return pick_j<DT, 2>(J, zp, two);
-  if (sb == 2) return pick_j<DT, 1>(J, zp, two);
-  return pick_j<DT, 0>(J, zp, two);
+KernelFn pick_dt(int J, bool zp, bool two, int sb, int ncg) {
+  return ncg == 1 ? pick_sb<DT, 1>(J, zp, two, sb) : pick_sb<DT, 2>(J, zp, two, sb);
 }
-KernelFn pick(int dtype, int J, bool zp, bool two, int sb) {
-  return dtype == W4A16_BF16 ? pick_dt<BF16>(J, zp, two, sb) : pick_dt<F16>(J, zp, two, sb);
+KernelFn pick(int dtype, int J, bool zp, bool two, int sb, int ncg) {
+  return dtype == W4A16_BF16 ? pick_dt<BF16>(J, zp, two, sb, ncg) : pick_dt<F16>(J, zp, two, sb, ncg);
+}
+int smem_of(int J, int ncg) {
+  if (ncg == 1) return J == 1 ? Layout<1, 1>::kSmem : Layout<2, 1>::kSmem;
+  return J == 1 ? Layout<1, 2>::kSmem : Layout<2, 2>::kSmem;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -512,29 +585,30 @@ bool decode_supported_impl(const GemmArgs &g) {
 }
 
 // CTAs of one decode kernel that can be resident at once when launched in clusters of C
-// (0 when unknown: no device). Queried from the runtime once per device and cluster size.
-int64_t resident_ctas(int J, int C) {
+// (0 when unknown: no device). Queried from the runtime once per device, variant and cluster size.
+int64_t resident_ctas(int J, int C, int ncg) {
   static std::mutex mu;
-  static int cache[64][2][kMaxCluster + 1];
-  static bool have[64][2][kMaxCluster + 1] = {};
+  static int cache[64][2][2][kMaxCluster + 1];
+  static bool have[64][2][2][kMaxCluster + 1] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (!have[dev][J - 1][C]) {
-    const KernelFn fn = pick(W4A16_F16, J, true, false, 1);  // occupancy does not depend on the stage size
-    const int smem = J == 1 ? Layout<1>::kSmem : Layout<2>::kSmem;
+  if (!have[dev][J - 1][ncg - 1][C]) {
+    const KernelFn fn = pick(W4A16_F16, J, true, false, 1, ncg);  // occupancy does not depend on the stage size
+    const int smem = smem_of(J, ncg);
+    const int threads = threads_of(ncg);
     int n = 0;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
         (C <= 8 || cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess)) {
       if (C == 1) {
         int per_sm = 0, sms = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) == cudaSuccess &&
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) == cudaSuccess &&
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
           n = per_sm * sms;
       } else {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(C), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(threads, 1, 1);
         cfg.dynamicSmemBytes = static_cast<size_t>(smem);
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -548,20 +622,34 @@ int64_t resident_ctas(int J, int C) {
       }
     }
     cudaGetLastError();  // a failed query leaves no sticky state
-    cache[dev][J - 1][C] = n;
-    have[dev][J - 1][C] = true;
+    cache[dev][J - 1][ncg - 1][C] = n;
+    have[dev][J - 1][ncg - 1][C] = true;
   }
-  return cache[dev][J - 1][C];
+  return cache[dev][J - 1][ncg - 1][C];
 }
 
+#ifdef W4A16_PROBE
+// Tuning builds only: force the consumer-group count, the split-K factor and the stage size.
+int g_probe_ncg = 0, g_probe_c = 0, g_probe_sb = 0;
+#endif
+
 }  // namespace
+
+#ifdef W4A16_PROBE
+extern "C" void w4a16_probe_decode_force(int ncg, int c, int sb) {
+  g_probe_ncg = ncg;
+  g_probe_c = c;
+  g_probe_sb = sb;
+}
+#endif
 
 // Pipeline shape for a cluster rank holding `kb` K blocks: blocks per stage (bigger TMA boxes move
 // data faster, but a CTA with few blocks needs small stages to start early), and the rank's range
 // rounded up to whole stages so that every stage starts on a multiple of 64 * sb rows.
-static void rank_shape(int64_t kbt, int C, int *sb, int64_t *kb_per_cta) {
+static void rank_shape(int64_t kbt, int C, int *sb, int64_t *kb_per_cta, int force_sb = 0) {
   int64_t kb = (kbt + C - 1) / C;
-  const int b = kb >= 16 ? 4 : 1;  // two-block stages measured slower than one-block ones here
+  int b = kb >= 16 ? 4 : 1;
+  if (force_sb) b = force_sb;
   kb = (kb + b - 1) / b * b;
   *sb = b;
   *kb_per_cta = kb;
@@ -577,6 +665,7 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
   // fixed latency (launch, first TMA round trip, cluster reduction) plus its K blocks; the number of
   // CTAs resident at once comes from the runtime's occupancy query (one per SM when unknown).
   constexpr double kFixedUs = 2.5, kPerBlockUs = 0.2;
+  int ncg = 2;
   int bestC = 1, bestSB = 1;
   double best = -1.0;
   for (int Ct = 1; Ct <= kMaxCluster; ++Ct) {
@@ -586,7 +675,7 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
     const int C = static_cast<int>((kbt + kb - 1) / kb);  // ranks left after rounding to whole stages
     if (C != Ct) continue;                                 // the same plan as a smaller C
     if (C > 1 && kb < 2) break;                            // every rank keeps at least two K blocks
-    int64_t slots = query_device ? resident_ctas(J, C) : 0;
+    int64_t slots = query_device ? resident_ctas(J, C, ncg) : 0;
     if (slots <= 0) slots = C <= 8 ? int64_t(num_sms) / C * C : 0;
     if (slots <= 0) continue;
     const int64_t ctas = n_tiles * C;
@@ -598,53 +687,75 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
       bestSB = sb;
     }
   }
+#ifdef W4A16_PROBE
+  if (g_probe_ncg) ncg = g_probe_ncg;
+  if (g_probe_c) {
+    int64_t kb = kbt;
+    rank_shape(kbt, g_probe_c, &bestSB, &kb, g_probe_sb);
+    bestC = static_cast<int>((kbt + kb - 1) / kb);
+  }
+#endif
   p->path = W4A16_PATH_DECODE;
   p->k_blocks_per_stage = bestSB;
   p->m_tile = 8 * J;
   p->n_tile = BN;
   p->k_split = static_cast<int32_t>(bestC);
-  p->warps = kConsumers + 1;
+  p->warps = kBlocksPerRow * ncg + 1;
   p->grid = n_tiles * bestC;
-  p->smem_bytes = J == 1 ? Layout<1>::kSmem : Layout<2>::kSmem;
+  p->smem_bytes = smem_of(J, ncg);
   p->stream_k = 0;
 }
 
 bool decode_supported(const GemmArgs &g) { return decode_supported_impl(g); }
 
-cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
+bool decode_weight_maps(const GemmArgs &g, const w4a16_plan_t &pl, WeightMaps *wm) {
+  const int sb = pl.k_blocks_per_stage;
+  const int srows = g.group_size < BK * sb ? BK * sb / g.group_size : 1;
+  const int64_t NW = g.N / 8, ng = g.K / g.group_size;
+  if (!tma_encode_2d(&wm->tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK * sb, true) ||
+      !tma_encode_2d(&wm->tS, 2, g.scales, g.N, ng, g.N * 2, BN, srows, false))
+    return false;
+  if (g.qzeros) {
+    if (!tma_encode_2d(&wm->tZ, 4, g.qzeros, NW, ng, NW * 4, BN / 8, srows, false)) return false;
+  } else {
+    wm->tZ = wm->tP;  // unused
+  }
+  wm->key = sb;
+  return true;
+}
+
+cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl, const WeightMaps *wm) {
   const int J = pl.m_tile / 8;
   const int C = pl.k_split;
+  const int ncg = (pl.warps - 1) / kBlocksPerRow;
   const bool zp = g.qzeros != nullptr;
   const bool two = g.group_size < BK && g.group_size != g.K;  // G = 32: two groups per K block
   const int64_t kbt = (g.K + BK - 1) / BK;
-  int sb = 1;
-  int64_t kb_per_cta = kbt;
-  rank_shape(kbt, C, &sb, &kb_per_cta);
-  if (sb != pl.k_blocks_per_stage || (kbt + kb_per_cta - 1) / kb_per_cta != C) return cudaErrorInvalidValue;
+  const int sb = pl.k_blocks_per_stage;
+  if (sb != 1 && sb != 2 && sb != 4) return cudaErrorInvalidValue;
+  // the rank's range of K blocks, rounded up to whole stages
+  const int64_t kb_per_cta = ((kbt + C - 1) / C + sb - 1) / sb * sb;
+  if ((kbt + kb_per_cta - 1) / kb_per_cta != C || (ncg != 1 && ncg != 2)) return cudaErrorInvalidValue;
   // scale / zero-point rows per stage: the groups of 64 * sb rows (G in {32, 64, 128} divides that
   // when it is smaller; a larger G, or G = K, leaves one group per stage)
   const int srows = g.group_size < BK * sb ? BK * sb / g.group_size : 1;
-  const int64_t NW = g.N / 8, ng = g.K / g.group_size;
-  CUtensorMap tA, tP, tS, tZ;
-  if (!tma_encode_2d(&tA, 2, g.a, g.K, g.M, g.K * 2, BK, 8 * J, true) ||
-      !tma_encode_2d(&tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK * sb, true) ||
-      !tma_encode_2d(&tS, 2, g.scales, g.N, ng, g.N * 2, BN, srows, false))
-    return cudaErrorInvalidValue;
-  if (zp) {
-    if (!tma_encode_2d(&tZ, 4, g.qzeros, NW, ng, NW * 4, BN / 8, srows, false)) return cudaErrorInvalidValue;
-  } else {
-    tZ = tP;  // unused
+  CUtensorMap tA;
+  if (!tma_encode_2d(&tA, 2, g.a, g.K, g.M, g.K * 2, BK, 8 * J, true)) return cudaErrorInvalidValue;
+  WeightMaps own;
+  if (!wm || wm->key != sb) {
+    if (!decode_weight_maps(g, pl, &own)) return cudaErrorInvalidValue;
+    wm = &own;
   }
-  const KernelFn fn = pick(g.dtype, J, zp, two, sb);
-  const int smem = J == 1 ? Layout<1>::kSmem : Layout<2>::kSmem;
+  const KernelFn fn = pick(g.dtype, J, zp, two, sb, ncg);
+  const int smem = smem_of(J, ncg);
   {
     static std::mutex mu;
-    static bool configured[64][2][2][2][2][3] = {};
+    static bool configured[64][2][2][2][2][3][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
-    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][J - 1][zp][two][sb == 4 ? 2 : sb - 1];
+    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][J - 1][zp][two][sb == 4 ? 2 : sb - 1][ncg - 1];
     if (!done) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
@@ -667,11 +778,14 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
   prm.srows = srows;
   // a stage of 64 * sb rows spans several groups only for G in {32, 64, 128} below that size
   prm.g_shift = g.group_size < BK * sb ? (g.group_size == 32 ? 5 : (g.group_size == 64 ? 6 : 7)) : 31;
+  // scale groups of 64 or 128 rows end on K-block boundaries; a larger group (G = K) is cut only by
+  // the stage ends
+  prm.bpg = (g.group_size == 64 || g.group_size == 128) ? g.group_size / BK : 0;
 
   const int64_t n_tiles = (g.N + BN - 1) / BN;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(n_tiles * C), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_of(ncg), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = g.stream;
   cudaLaunchAttribute attr[2];
@@ -688,7 +802,7 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tA, tP, tS, tZ, prm);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tA, wm->tP, wm->tS, wm->tZ, prm);
   if (e != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;

@@ -170,6 +170,7 @@ struct PrefillParams {
   unsigned int *flags;  // stream-K: per-CTA "partial ready" flags; zero before and after every launch
   int csplit;        // > 1: clusters of csplit CTAs split each tile's K blocks (128-row tiles only)
   int a_rows;        // rows of A per TMA box: BM, or M rounded up to 8 when one row tile covers M
+  int dp_waves;      // stream-K: whole waves of tiles done data-parallel first (CTA c: c, c + G, ...)
 };
 
 // First (tile, K block) work unit of CTA c when the tiles x nk units are split evenly over G CTAs.
@@ -224,30 +225,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work units are (tile, K block) pairs, tile-major; CTA c takes a contiguous, even share. With one
-  // CTA per tile every share is a whole tile; with fewer CTAs (stream-K) a share may start or end
-  // inside a tile: the CTA holding a tile's K block 0 owns it and adds the partial tiles of the
-  // CTAs that hold the rest (they publish them in the workspace) before the epilogue.
+  // Work units are (tile, K block) pairs. Stream-K plans first run dp_waves whole waves of tiles
+  // data-parallel: CTA c takes tiles c, c + G, c + 2G, ..., so the CTAs of a wave step through K
+  // together over neighbouring tiles (row tiles fastest) and share the A and weight slices in L2.
+  // The remaining tiles' units, tile-major, are then split into contiguous, even shares (with one CTA
+  // per tile every share is a whole tile): a share may start or end inside a tile; the CTA holding a
+  // tile's K block 0 owns it and adds the partial tiles of the CTAs that hold the rest (they publish
+  // them in the workspace) before the epilogue.
   const int nk = p.nk;
-  const int64_t total = p.tiles * nk;
   const int64_t G = gridDim.x;
   // Cluster split-K: the C CTAs of a cluster share one tile, rank r taking K blocks
   // [r nk / C, (r + 1) nk / C); their partial tiles meet in distributed shared memory.
   const int C = p.csplit;
+  const int64_t dp_tiles = C > 1 ? 0 : int64_t(p.dp_waves) * G;  // tiles done data-parallel
+  const int dp_units = C > 1 ? 0 : p.dp_waves * nk;              // this CTA's data-parallel units
+  const int64_t total = (p.tiles - dp_tiles) * nk;                // units shared out after them
+  // this CTA's share, in units counted from the first shared tile
   const int64_t u_begin = C > 1 ? (blockIdx.x / C) * int64_t(nk) + int64_t(blockIdx.x % C) * nk / C
                                 : unit_begin(blockIdx.x, total, G);
   const int64_t u_end = C > 1 ? (blockIdx.x / C) * int64_t(nk) + int64_t(blockIdx.x % C + 1) * nk / C
                               : unit_begin(int64_t(blockIdx.x) + 1, total, G);
-  const int n_units = static_cast<int>(u_end - u_begin);
-  const int64_t t_first = u_begin / nk;
-  const int kb_first = static_cast<int>(u_begin - t_first * nk);
+  const int n_units = dp_units + static_cast<int>(u_end - u_begin);
+  const int kb_first = static_cast<int>(u_begin % nk);
+  // Tile and K block of this CTA's unit i.
+  auto unit_at = [&](int i, int64_t &t, int &kb) {
+    if (i < dp_units) {
+      t = int64_t(blockIdx.x) + int64_t(i / nk) * G;
+      kb = i % nk;
+    } else {
+      const int64_t u = u_begin + (i - dp_units);
+      t = dp_tiles + u / nk;
+      kb = static_cast<int>(u % nk);
+    }
+  };
   // The share's last segment needs a fix-up when it starts a tile (K block 0) but ends inside it: the
   // CTAs after this one hold the rest of that tile and publish their partial tiles.
-  const int64_t t_last = n_units > 0 ? (u_end - 1) / nk : t_first;
-  const bool fix_needed = C == 1 && n_units > 0 && (t_last > t_first || kb_first == 0) && u_end < (t_last + 1) * nk;
-  int64_t c_fix = blockIdx.x;  // last CTA holding part of tile t_last
+  const int64_t s_first = u_begin / nk;  // first and last shared tile, counted from dp_tiles
+  const int64_t s_last = u_end > u_begin ? (u_end - 1) / nk : s_first;
+  const bool fix_needed =
+      C == 1 && u_end > u_begin && (s_last > s_first || kb_first == 0) && u_end < (s_last + 1) * nk;
+  int64_t c_fix = blockIdx.x;  // last CTA holding part of tile s_last
   if (fix_needed)
-    while (c_fix + 1 < G && unit_begin(c_fix + 1, total, G) < (t_last + 1) * nk) ++c_fix;
+    while (c_fix + 1 < G && unit_begin(c_fix + 1, total, G) < (s_last + 1) * nk) ++c_fix;
   const int n_con = static_cast<int>(c_fix - blockIdx.x);  // contributors to add
 
   const uint32_t bar0 = base + kOffBar;
@@ -334,23 +353,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       // other ring in steady state, and every wait depends only on work already requested.
       constexpr int kLag = kShared ? 0 : SP - SA;
       int issued_p = 0, issued_a = 0;
-      int64_t tp = t_first, ta = t_first;
-      int kbp = kb_first, kba = kb_first;
       auto issue_a = [&](int j) -> bool {
         const int s = j % SA;
         if (!wait_phase(empty_a(s), ((j / SA) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error)) return false;
+        int64_t ta;
+        int kba;
+        unit_at(j, ta, kba);
         mbar_arrive_expect_tx(full_a(s), tx_a);
         tma_load_2d(base + kOffA + s * kABytes, &tmA, kba * BK, static_cast<int>((ta % p.m_tiles) * BM), full_a(s));
         issued_a = j + 1;
-        if (++kba == nk) {
-          kba = 0;
-          ++ta;
-        }
         return true;
       };
       bool run = true;
       for (int j = 0; j < n_units && run; ++j) {
         const int s = j % SP;
+        int64_t tp;
+        int kbp;
+        unit_at(j, tp, kbp);
         run = wait_phase(empty_p(s), ((j / SP) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error);
         if (!run) break;
         if constexpr (kShared) {
@@ -368,10 +387,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(base + kOffS + s * kSBytes, &tmS, n0, grow, full_p(s));
         if constexpr (HAS_ZP) tma_load_2d(base + kOffZ + s * kZBytes, &tmZ, n0 / 8, grow, full_p(s));
         issued_p = j + 1;
-        if (++kbp == nk) {
-          kbp = 0;
-          ++tp;
-        }
         if (!kShared && j >= kLag) run = issue_a(j - kLag);
       }
       if constexpr (!kShared)
@@ -429,10 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                              | (uint32_t(BN >> 3) << 17)       // N
                              | (uint32_t(128 >> 4) << 24);     // M (one MMA per 128-row half)
       bool ok = true;
-      int kb = kb_first, seg = 0;
+      int seg = 0;
       bool seg_start = true;
       for (int i = 0; i < n_units && ok; ++i) {
         const int sa = i % SA, sb = i % SB;
+        int64_t ti;
+        int kb;
+        unit_at(i, ti, kb);
         if (seg_start && seg > 0) {
           // the epilogue of the previous segment has read the accumulators out of TMEM
           ok = wait_phase(accum_empty, (seg - 1) & 1, abort_flag, limit_ns, &g_prefill_error);
@@ -466,7 +484,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++seg;
           seg_start = true;
         }
-        if (++kb == nk) kb = 0;
       }
       if (!ok) {
         umma_commit(accum_full);
@@ -499,10 +516,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = wait_phase(stall_bar, 0, abort_flag, limit_ns, &g_prefill_error);
       ok = __all_sync(0xffffffffu, ok);
     }
-    int64_t t = t_first;
-    int kb = kb_first, seg = 0, seg_kb0 = kb_first, epi_uses = 0;
+    int seg = 0, seg_kb0 = 0, epi_uses = 0;
+    bool seg_open = false;  // a segment (one tile's run of K blocks) has started
     const int dgrp = dw / kGroupWarps, dwg = dw % kGroupWarps;  // dequantiser group, warp within it
     for (int i = 0; i < n_units && ok; ++i) {
+      int64_t t;
+      int kb;
+      unit_at(i, t, kb);
+      if (!seg_open) {
+        seg_kb0 = kb;  // K block the segment starts at: 0 unless a share starts inside the tile
+        seg_open = true;
+      }
       if (i % kDqGroups == dgrp) {
         const int sp = i % SP, sb = i % SB;
         ok = wait_phase(full_p(sp), (i / SP) & 1, abort_flag, limit_ns, &g_prefill_error) &&
@@ -718,11 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         ++seg;
-        seg_kb0 = 0;
-      }
-      if (++kb == nk) {
-        kb = 0;
-        ++t;
+        seg_open = false;
       }
     }
     // this warp's TMEM reads are complete (each tcgen05.ld was waited on): release the accumulators
@@ -890,6 +910,16 @@ static int64_t cluster_slots(int C) {
   return cache[dev][C];
 }
 
+// Stream-K plans run whole waves of tiles data-parallel first. The remaining tiles' units are shared
+// out evenly, which needs at least one unit per CTA (a CTA with an empty share would never publish
+// the partial tile its tile's owner waits for): with fewer, one wave fewer runs data-parallel.
+int prefill_dp_waves(int64_t tiles, int64_t nk, int64_t grid) {
+  int64_t w = tiles / grid;
+  const int64_t rem = tiles - w * grid;
+  if (w > 0 && rem > 0 && rem * nk < grid) --w;
+  return static_cast<int>(w);
+}
+
 void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool workspace,
                        bool query_device, w4a16_plan_t *p) {
   (void)group_size;
@@ -926,8 +956,10 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
       const int64_t total = tiles * nk;
       const double step = mt == 1 ? 0.7 : 1.0, fix = 3.0;
       for (int64_t g = 1; g <= std::min<int64_t>(std::min<int64_t>(sms, kMaxStreamKCtas), total); ++g) {
-        const int64_t share = (total + g - 1) / g;
-        const int64_t parts = (g + tiles - 1) / tiles + 1;  // CTAs touching one tile, at most
+        // whole waves data-parallel, then the remaining tiles' units in even shares
+        const int64_t waves = prefill_dp_waves(tiles, nk, g), rem = tiles - waves * g;
+        const int64_t share = waves * nk + (rem * nk + g - 1) / g;
+        const int64_t parts = rem > 0 ? (g + rem - 1) / rem + 1 : 1;  // CTAs touching one shared tile, at most
         const double cost = double(share) * step + fix * double(parts - 1);
         if (cost < best - 1e-9) {
           best = cost;
@@ -967,24 +999,35 @@ void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_
   p->stream_k = stream_k ? 1 : 0;
 }
 
-cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl) {
-  const int MT = pl.m_tile / 128;
-  const int BM = 128 * MT;
-  const bool zp = g.qzeros != nullptr;
+bool prefill_weight_maps(const GemmArgs &g, WeightMaps *wm) {
   const int64_t NW = g.N / 8, ng = g.K / g.group_size;
   const bool two = g.group_size < BK && g.group_size != g.K;  // G = 32: two groups per K block
   const int srows = two ? 2 : 1;
+  if (!tma_encode_2d(&wm->tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK, false) ||
+      !tma_encode_2d(&wm->tS, 2, g.scales, g.N, ng, g.N * 2, BN, srows, false))
+    return false;
+  if (g.qzeros) {
+    if (!tma_encode_2d(&wm->tZ, 4, g.qzeros, NW, ng, NW * 4, BN / 8, srows, false)) return false;
+  } else {
+    wm->tZ = wm->tP;  // unused
+  }
+  wm->key = 0;
+  return true;
+}
+
+cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl, const WeightMaps *wm) {
+  const int MT = pl.m_tile / 128;
+  const int BM = 128 * MT;
+  const bool zp = g.qzeros != nullptr;
+  const bool two = g.group_size < BK && g.group_size != g.K;  // G = 32: two groups per K block
   // one row tile: fetch only the rows up to M (rounded up to 8) of each A block
   const int a_rows = g.M <= BM ? static_cast<int>((g.M + 7) / 8 * 8) : BM;
-  CUtensorMap tA, tP, tS, tZ;
-  if (!tma_encode_2d(&tA, 2, g.a, g.K, g.M, g.K * 2, BK, a_rows, true) ||
-      !tma_encode_2d(&tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK, false) ||
-      !tma_encode_2d(&tS, 2, g.scales, g.N, ng, g.N * 2, BN, srows, false))
-    return cudaErrorInvalidValue;
-  if (zp) {
-    if (!tma_encode_2d(&tZ, 4, g.qzeros, NW, ng, NW * 4, BN / 8, srows, false)) return cudaErrorInvalidValue;
-  } else {
-    tZ = tP;  // unused
+  CUtensorMap tA;
+  if (!tma_encode_2d(&tA, 2, g.a, g.K, g.M, g.K * 2, BK, a_rows, true)) return cudaErrorInvalidValue;
+  WeightMaps own;
+  if (!wm) {
+    if (!prefill_weight_maps(g, &own)) return cudaErrorInvalidValue;
+    wm = &own;
   }
   const KernelFn fn = pick(g.dtype, zp, two, MT);
   {
@@ -1024,6 +1067,7 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl) {
   prm.nk = static_cast<int>((g.K + BK - 1) / BK);
   prm.csplit = pl.k_split > 1 ? pl.k_split : 1;
   prm.a_rows = a_rows;
+  prm.dp_waves = pl.stream_k ? prefill_dp_waves(prm.tiles, prm.nk, pl.grid) : 0;
   if (prm.csplit > 1 && (MT != 1 || pl.stream_k || pl.grid % prm.csplit != 0 || prm.nk < prm.csplit))
     return cudaErrorInvalidValue;
 
@@ -1046,7 +1090,7 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tA, tP, tS, tZ, prm);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tA, wm->tP, wm->tS, wm->tZ, prm);
   if (e != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;

@@ -35,6 +35,9 @@ struct DeviceInfo {
 // Cached per-device properties of the current device (queried once per device).
 cudaError_t current_device_info(DeviceInfo *info);
 
+// The dispatcher's plan for a call (kept per shape, dtype, alignment, workspace offer and device).
+void cached_plan(const GemmArgs &g, const DeviceInfo &dev, bool workspace, w4a16_plan_t *plan);
+
 // Records one kernel launch in the process-wide counter.
 void note_launch();
 
@@ -54,12 +57,23 @@ cudaError_t launch_dequant(const int32_t *b_q, const void *scales, const int32_t
 
 cudaError_t launch_gemm_generic(const GemmArgs &g);
 
+// TMA descriptors of a layer's weights (packed weights, scales, zero points), encoded once by a
+// prepared layer and reused by its calls. `key` names the box shape they were encoded for (decode:
+// K blocks per stage; prefill: 0).
+struct WeightMaps {
+  CUtensorMap tP, tS, tZ;
+  int key;
+};
+
 // Decode path (M <= 16): plan fields m_tile and k_split are honoured.
 bool decode_supported(const GemmArgs &g);
 // query_device: use the runtime's occupancy queries (needs a device); otherwise assume 2 CTAs per SM.
 void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool query_device,
                       w4a16_plan_t *p);
-cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &p);
+// Weight descriptors for a decode plan; false when the driver rejects them.
+bool decode_weight_maps(const GemmArgs &g, const w4a16_plan_t &p, WeightMaps *wm);
+// wm: weight descriptors encoded for this plan, or null (encoded per call).
+cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &p, const WeightMaps *wm = nullptr);
 cudaError_t decode_take_device_error(uint32_t *err);
 cudaError_t decode_set_wait_limit_ns(uint64_t ns);
 cudaError_t decode_set_stall(bool on);
@@ -70,12 +84,15 @@ bool prefill_supported(const GemmArgs &g);
 void prefill_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool workspace,
                        bool query_device, w4a16_plan_t *p);
 size_t prefill_workspace_bytes(int64_t M, int64_t K, int64_t N, int group_size, int num_sms);
+// Whole waves of tiles a stream-K plan over `grid` CTAs runs data-parallel before the shared units.
+int prefill_dp_waves(int64_t tiles, int64_t nk, int64_t grid);
 // Workspace bytes a prefill plan needs (0 unless it is stream-K).
 size_t prefill_plan_workspace_bytes(const w4a16_plan_t &plan);
 // Device address and size of the library's static scratch array on the current device (looked up
 // once per device).
 cudaError_t prefill_static_scratch(void **ptr, size_t *bytes);
-cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &p);
+bool prefill_weight_maps(const GemmArgs &g, WeightMaps *wm);
+cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &p, const WeightMaps *wm = nullptr);
 // Reads and clears the device error word of the prefill kernels on the current device.
 cudaError_t prefill_take_device_error(uint32_t *err);
 cudaError_t prefill_set_wait_limit_ns(uint64_t ns);
