@@ -268,6 +268,16 @@ int w4a16_debug_selected_path(int64_t m, int64_t k, int64_t n, int group_size);
 w4a16_status w4a16_debug_force_path(int path);
 
 /*
+ * w4a16_debug_decode_override - fixes parts of the decode path's launch plan for tests and tuning:
+ * consumer_groups (1: one group of eight consumer warps per CTA and an 8-block ring, so that two CTAs
+ * fit on an SM; 2: two groups and a 16-block ring), k_split (the CTAs of a cluster that split K,
+ * 1..16; the rank ranges are rounded to whole stages, which may leave fewer ranks) and
+ * k_blocks_per_stage (1, 2 or 4). 0 leaves a field to the dispatcher; all zero restores the
+ * automatic plan. Process-wide. Errors: INVALID_ARG for values outside those ranges.
+ */
+w4a16_status w4a16_debug_decode_override(int consumer_groups, int k_split, int k_blocks_per_stage);
+
+/*
  * w4a16_debug_set_wait_limit_ns - sets the limit of every bounded device-side wait (nanoseconds;
  * 0 restores the default of 2 s). A test sets a tiny limit to make a wait give up and checks that
  * the TIMEOUT status is reported without hanging the GPU. Synchronous.

@@ -109,14 +109,14 @@ def test_dispatcher_decode_for_small_m_and_split_k(w):
             p = w.w4a16_plan(m, k, n, 32 if k in (1152, 2112) else 128, 0, False, 152)
             assert p["path_name"] == "decode", (m, k, n, p)
             assert p["m_tile"] == 8
-            assert 1 <= p["k_split"] <= 8
+            assert 1 <= p["k_split"] <= 16
             assert p["grid"] <= 2 * 152
     # a narrow layer gets split along K across a cluster
     p = w.w4a16_plan(1, 2112, 1152, 32, 1, False, 152)
     assert p["k_split"] > 1
-    # a wide one is split only as far as needed to fill two CTAs per SM
+    # a wide one is split only as far as needed to put one CTA on every SM
     p = w.w4a16_plan(1, 2560, 19456, 128, 0, True, 152)
-    assert p["k_split"] <= 4 and 152 <= p["grid"] <= 304
+    assert p["k_split"] <= 2 and 76 <= p["grid"] <= 152
     # and the choice follows the device: half the SMs, half the CTAs
     assert w.w4a16_plan(1, 2560, 19456, 128, 0, True, 76)["grid"] <= 152
 
@@ -207,3 +207,28 @@ def test_layer_handle_validation_without_a_device(w):
 def test_force_path_entry_point_validates(w):
     assert w.lib().w4a16_debug_force_path(7) == 1
     assert w.lib().w4a16_debug_force_path(-1) == 0
+
+
+# Decode plans the dispatcher picks on a 152-SM GB300 for the decode workloads' layers, against the
+# plans that measured fastest there (per-call time of CUDA-graph chains of calls over rotating weight
+# replicas, every split-K factor 1..16 tried with one and two consumer groups and stages of one and
+# two K blocks; M = 1 and M = 8): one consumer group (9 warps), one K block per stage, and this
+# split-K factor.
+MEASURED_BEST_DECODE_SPLIT = {
+    (1152, 4224, 32): 6,     # 102 CTAs, 2.8 us
+    (2112, 1152, 32): 11,    # 55 CTAs, 2.7-2.9 us
+    (2560, 3840, 128): 10,   # 150 CTAs, 4.2-4.4 us
+    (2560, 19456, 128): 2,   # 152 CTAs, 8.8-9.1 us
+    (9728, 2560, 128): 14,   # 140 CTAs
+}
+
+
+@pytest.mark.parametrize("shape", sorted(MEASURED_BEST_DECODE_SPLIT))
+def test_decode_planner_picks_the_measured_best_plan(w, shape):
+    K, N, G = shape
+    for M in (1, 2, 4, 5, 8):
+        for dt, zp in ((0, True), (1, False)):
+            p = w.w4a16_plan(M, K, N, G, dt, zp, 152, False)
+            assert p["path_name"] == "decode"
+            assert (p["warps"], p["k_split"], p["k_blocks_per_stage"]) == (9, MEASURED_BEST_DECODE_SPLIT[shape], 1), p
+            assert p["grid"] == -(-N // 256) * p["k_split"]

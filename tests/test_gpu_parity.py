@@ -398,3 +398,47 @@ def test_cluster_split_k_mid_m(w, M, K, N, G, dt, asym):
     check_against_oracle(c, outs[0], rows=rows, cols=sample_cols(N, rng, k=128), label="cluster split-K",
                          path="prefill")
 
+
+
+DECODE_VARIANTS = [(ncg, C, sb) for ncg in (1, 2) for (C, sb) in ((1, 4), (2, 2), (3, 1), (5, 2), (9, 1), (16, 1), (2, 4))]
+
+
+@pytest.mark.parametrize("M,K,N,G,dt,asym,bias", [(1, 1152, 4224, 32, "bf16", False, False),
+                                                 (5, 2112, 1152, 32, "bf16", False, False),
+                                                 (8, 2560, 3840, 128, "f16", True, True),
+                                                 (3, 5120, 1024, 5120, "bf16", True, False),
+                                                 (16, 1024, 2048, 64, "f16", False, True),
+                                                 (12, 4104, 288, 4104, "f16", True, True)])
+def test_every_decode_configuration_matches_oracle(w, M, K, N, G, dt, asym, bias):
+    """Each decode configuration (one or two consumer groups, split-K factors up to 16 with the
+    split-K exchange through st.async pushes, stages of 1, 2 or 4 K blocks) against the oracle on the
+    exact-weight reading, and the identity-A product bit-exact, on shapes with ragged K and N."""
+    if N % 32:
+        pytest.skip("decode needs N % 32 == 0")
+    c = synth.make_case(M, K, N, G, dt, asym=asym, bias=bias, seed=M * 3 + K)
+    t = case_tensors(c)
+    one = int(oracle.ieee.t_encode_rne(np.array([1.0]), dt)[0])
+    ks = np.random.default_rng(M).choice(K, size=M, replace=False)
+    a_id = c.a.copy()
+    a_id[:] = 0
+    a_id[np.arange(M), ks] = one
+    t_id = bits_to_torch(a_id, dt)
+    want_id = oracle.dequant_t(c.b_q, c.scales, c.qzeros, G, 8, dt)[ks]
+    seen = set()
+    try:
+        for ncg, C, sb in DECODE_VARIANTS:
+            w.w4a16_debug_decode_override(ncg, C, sb)
+            plan = w.w4a16_plan(M, K, N, G, 1 if dt == "bf16" else 0, asym, 0, with_workspace=False)
+            assert plan["path_name"] == "decode"
+            key = (plan["warps"], plan["k_split"], plan["k_blocks_per_stage"])
+            if key in seen:
+                continue
+            seen.add(key)
+            out = w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"], use_workspace=False)
+            out_id = w.w4a16_gemm(t_id, t["b_q"], t["scales"], t["qzeros"], G, 8, None, use_workspace=False)
+            torch.cuda.synchronize()
+            check_against_oracle(c, torch_to_bits(out), label=f"decode plan {key}", path="decode")
+            assert np.array_equal(torch_to_bits(out_id), want_id), f"identity A, decode plan {key}"
+    finally:
+        w.w4a16_debug_decode_override(0, 0, 0)
+    assert w.w4a16_get_device_error() == 0

@@ -68,6 +68,7 @@ SIGNATURES = [
     ("w4a16_get_device_error", _c_int, []),
     ("w4a16_debug_selected_path", _c_int, [_c_i64, _c_i64, _c_i64, _c_int]),
     ("w4a16_debug_force_path", _c_int, [_c_int]),
+    ("w4a16_debug_decode_override", _c_int, [_c_int, _c_int, _c_int]),
     ("w4a16_debug_set_wait_limit_ns", _c_int, [ctypes.c_uint64]),
     ("w4a16_debug_inject_stall", _c_int, [_c_int]),
     ("w4a16_debug_launch_count", ctypes.c_uint64, []),
@@ -363,6 +364,11 @@ def w4a16_debug_force_path(path):
     _check(lib().w4a16_debug_force_path(code))
 
 
+def w4a16_debug_decode_override(consumer_groups: int = 0, k_split: int = 0, k_blocks_per_stage: int = 0):
+    """Fix the decode plan's consumer groups, split-K factor and stage size (0: automatic)."""
+    _check(lib().w4a16_debug_decode_override(consumer_groups, k_split, k_blocks_per_stage))
+
+
 def w4a16_debug_set_wait_limit_ns(ns: int):
     _check(lib().w4a16_debug_set_wait_limit_ns(ns))
 
@@ -382,6 +388,7 @@ def w4a16_version() -> str:
 __all__ = ["w4a16_pack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_can_implement", "w4a16_plan",
            "w4a16_gemm_workspace_size", "workspace_for",
            "w4a16_get_device_error", "w4a16_debug_selected_path", "w4a16_debug_force_path",
+           "w4a16_debug_decode_override",
            "w4a16_debug_set_wait_limit_ns",
            "w4a16_debug_inject_stall",
            "w4a16_debug_launch_count", "w4a16_version", "W4A16Error", "lib", "last_error", "LIB_PATH",

@@ -81,6 +81,7 @@ w4a16_status check_config(int64_t K, int64_t N, int G, int dtype) {
 // w4a16_debug_force_path, initially from the environment variable W4A16_FORCE_PATH
 // (generic|decode|prefill), read once. -1: no restriction; -2: not read yet.
 std::atomic<int> g_forced_path{-2};
+std::atomic<uint64_t> g_plan_epoch{0};
 int forced_path() {
   int f = g_forced_path.load(std::memory_order_relaxed);
   if (f != -2) return f;
@@ -166,13 +167,20 @@ uint32_t plan_flags(const GemmArgs &g, bool workspace, bool tma) {
 
 }  // namespace
 
+uint64_t plan_epoch() { return g_plan_epoch.load(std::memory_order_relaxed); }
+
 void cached_plan(const GemmArgs &g, const DeviceInfo &dev, bool workspace, w4a16_plan_t *plan) {
   static std::mutex mu;
   static std::unordered_map<PlanKey, w4a16_plan_t, PlanKeyHash> plans;
+  static uint64_t epoch = 0;
   const bool tma = tma_available();
   const PlanKey key{g.M, g.K, g.N, g.group_size, g.dtype, dev.device, forced_path(), plan_flags(g, workspace, tma)};
   {
     std::lock_guard<std::mutex> lock(mu);
+    if (epoch != plan_epoch()) {  // a debug setting changed: plans made before it are stale
+      plans.clear();
+      epoch = plan_epoch();
+    }
     auto it = plans.find(key);
     if (it != plans.end()) {
       *plan = it->second;
@@ -462,6 +470,7 @@ struct w4a16_layer_st {
   };
   std::mutex mu;
   std::unordered_map<uint64_t, Entry> cache;  // key: M, plan flags, forced path
+  uint64_t epoch = 0;                          // plan_epoch() the entries were made under
 };
 
 extern "C" {
@@ -540,6 +549,10 @@ w4a16_status w4a16_layer_gemm(w4a16_layer_t layer, const void *a, void *out, int
     const uint64_t key = (uint64_t(m) << 20) | (uint64_t(plan_flags(g, ws, tma)) << 4) | uint64_t(force + 2);
     {
       std::lock_guard<std::mutex> lock(layer->mu);
+      if (layer->epoch != plan_epoch()) {
+        layer->cache.clear();
+        layer->epoch = plan_epoch();
+      }
       auto it = layer->cache.find(key);
       if (it != layer->cache.end()) return it->second;
     }
@@ -625,6 +638,17 @@ w4a16_status w4a16_debug_force_path(int path) {
   if (path != -1 && path != W4A16_PATH_GENERIC && path != W4A16_PATH_DECODE && path != W4A16_PATH_PREFILL)
     return fail(W4A16_ERR_INVALID_ARG, "path %d is not -1, W4A16_PATH_GENERIC, _DECODE or _PREFILL", path);
   g_forced_path.store(path, std::memory_order_relaxed);
+  g_plan_epoch.fetch_add(1, std::memory_order_relaxed);
+  return ok();
+}
+
+w4a16_status w4a16_debug_decode_override(int consumer_groups, int k_split, int k_blocks_per_stage) {
+  if (consumer_groups < 0 || consumer_groups > 2 || k_split < 0 || k_split > 16 ||
+      (k_blocks_per_stage != 0 && k_blocks_per_stage != 1 && k_blocks_per_stage != 2 && k_blocks_per_stage != 4))
+    return fail(W4A16_ERR_INVALID_ARG, "override out of range: consumer_groups in 0..2, k_split in 0..16, "
+                "k_blocks_per_stage in {0, 1, 2, 4}");
+  decode_set_override(consumer_groups, k_split, k_blocks_per_stage);
+  g_plan_epoch.fetch_add(1, std::memory_order_relaxed);
   return ok();
 }
 

@@ -171,6 +171,15 @@ __device__ __forceinline__ void st_async_f32(uint32_t cluster_addr, float v, uin
                "r"(__float_as_uint(v)), "r"(cluster_bar)
                : "memory");
 }
+// Asynchronous 16-byte store (16-byte aligned) into the shared memory of a CTA of the cluster, completion
+// counted in bytes on that CTA's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c, float d,
+                                            uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(cluster_addr),
+               "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
+               "r"(cluster_bar)
+               : "memory");
+}
 // Maps a shared::cta address of this CTA to the same offset in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
   uint32_t r;

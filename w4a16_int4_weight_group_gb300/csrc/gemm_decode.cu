@@ -36,6 +36,9 @@
 //    report, key source snippets, test reference).
 //  * Every mbarrier wait is bounded: on expiry the CTA records an error word, its warps leave the
 //    loop, the producer drains its own copies, and the CTA still takes part in the cluster barriers.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include "common.cuh"
@@ -92,10 +95,11 @@ struct Layout {
   static constexpr int kOffA = kOffP + R * kP;
   static constexpr int kOffS = kOffA + R * kA;
   static constexpr int kOffZ = kOffS + R * kS;
-  // Split-K receive buffer: this CTA's slice of the tile's live outputs from every (rank, consumer
-  // group), fp32, written by the other CTAs of the cluster (and by this one) with st.async. At most
-  // NCG x (8J x 256 + 16) floats: C slices of ceil(live / C) elements per contributor group.
-  static constexpr int kRecvFloats = NCG * (8 * J * BN + kMaxCluster);
+  // Split-K receive buffer: this CTA's slice of the tile's partial sums from every cluster rank,
+  // fp32 in groups of four, written by the ranks (this one included) with st.async: C slices of
+  // ceil(512 J / C) + 3 groups, at most 8J x 256 + 16 x 16 floats. Without a cluster it holds the second
+  // consumer group's partial tile instead.
+  static constexpr int kRecvFloats = 8 * J * BN + 16 * kMaxCluster;
   static constexpr int kOffRecv = kOffZ + R * kZ;
   static constexpr int kOffBar = kOffRecv + kRecvFloats * 4;
   // full[R], empty[R], the stall-test barrier, the receive barrier
@@ -185,13 +189,32 @@ __global__ void __launch_bounds__(threads_of(NCG), NCG == 1 ? 2 : W4A16_DEC_MINB
   const uint32_t full0 = base + L::kOffBar, empty0 = full0 + 8u * L::R;
   const uint32_t stall_bar = empty0 + 8u * L::R;
   const uint32_t recv_bar = stall_bar + 8u;
-  // Split-K exchange: the live outputs (rows below M) of the tile, flattened o = m * 256 + n, are cut
-  // into C slices of `per` elements; rank s adds slice s over every (rank, group) contribution.
+  // Split-K exchange across a cluster. A CTA's partial tile travels in accumulator order, four floats
+  // at a time: group g = ((w * 2 + q) * J + jt) * 32 + lane holds acc[jt][q][0..3] of consumer warp w.
+  // The 512 J groups are cut into C slices of per_g; rank s adds slice s over every rank. A group is
+  // live when its first row 8 jt + 2 (lane & 3) lies below M; only live groups travel.
   const int64_t rows = p.M < 8 * J ? p.M : 8 * J;
-  const bool push = C > 1 || NCG > 1;
-  const int live = static_cast<int>(rows) * BN;
-  const int per = (live + C - 1) / C;
-  const int my_per = max(0, min(per, live - rank * per));
+  const bool push = C > 1;  // only in a cluster launch
+  constexpr int kGroups4 = 512 * J;
+  const int per_g = ((kGroups4 + C - 1) / C + 3) & ~3;  // a multiple of 4 (whole tig cycles)
+  const int my_lo = min(kGroups4, rank * per_g), my_hi = min(kGroups4, my_lo + per_g);
+  // live groups among [0, x): lanes with tig < ceil((rows - 8 jt) / 2), in 32-lane runs per jt
+  auto live_below = [&](int x) {
+    const int rr = static_cast<int>(rows);
+    const int l0 = min(4, (rr + 1) / 2);
+    const int l1 = J == 2 ? max(0, min(4, (rr - 8 + 1) / 2)) : 0;
+    const int span = 32 * J;
+    const int per_span = 8 * l0 + (J == 2 ? 8 * l1 : 0);
+    const int r = x % span;
+    int c = (x / span) * per_span;
+    if (r < 32) {
+      c += (r / 4) * l0 + min(r % 4, l0);
+    } else {
+      c += 8 * l0 + ((r - 32) / 4) * l1 + min((r - 32) % 4, l1);
+    }
+    return c;
+  };
+  const int my_live = live_below(my_hi) - live_below(my_lo);
   const uint32_t abort_flag = base + L::kOffFlag;
   const unsigned long long lim = g_decode_wait_limit_ns;
   const uint64_t limit_ns = lim ? lim : kDefaultWaitNs;
@@ -209,7 +232,7 @@ __global__ void __launch_bounds__(threads_of(NCG), NCG == 1 ? 2 : W4A16_DEC_MINB
     st_flag(abort_flag, 0u);
     mbar_init_fence();
     // every contribution to this CTA's slice lands with st.async, counted in bytes on recv_bar
-    if (push) mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(C * NCG * my_per * 4));
+    if (push) mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(C * my_live * 16));
   }
   if (warp == kConsumers && lane == 0) {
     // descriptors live in the kernel parameters, not in memory an earlier kernel writes
@@ -491,6 +514,30 @@ __global__ void __launch_bounds__(threads_of(NCG), NCG == 1 ? 2 : W4A16_DEC_MINB
   };
   const int nl0 = 32 * (warp % kBlocksPerRow) + 4 * gl;
   if (!push) {
+    if constexpr (NCG == 2) {
+      // one CTA: group 1 hands its sums to group 0 through shared memory (the receive buffer is free
+      // without a cluster), fixed order group 0 + group 1
+      float *gred = reinterpret_cast<float *>(base_ptr + L::kOffRecv);
+      if (warp >= kBlocksPerRow && warp < kConsumers) {
+#pragma unroll
+        for (int jt = 0; jt < J; ++jt)
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) gred[(8 * jt + 2 * tig + (e & 1)) * BN + nl0 + q + 2 * (e >> 1)] = acc[jt][q][e];
+      }
+      // named barrier of the consumer warps only: the producer warp must not arrive on it (an extra
+      // warp would open a second phase of the barrier that nobody completes)
+      if (warp < kConsumers) asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+      if (warp < kBlocksPerRow) {
+#pragma unroll
+        for (int jt = 0; jt < J; ++jt)
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[jt][q][e] += gred[(8 * jt + 2 * tig + (e & 1)) * BN + nl0 + q + 2 * (e >> 1)];
+      }
+    }
     if (warp < kBlocksPerRow) {
       const int64_t nb = n0 + nl0;
 #pragma unroll
@@ -505,43 +552,78 @@ __global__ void __launch_bounds__(threads_of(NCG), NCG == 1 ? 2 : W4A16_DEC_MINB
         }
     }
   } else {
-    // Split-K (cluster ranks and consumer groups): every consumer pushes each of its live partial
-    // sums into the receive buffer of the rank that adds that output, at the slot of its (rank,
-    // group); no cluster barrier and no remote load sits between the last product and the sums.
-    // A CTA that gave up a wait pushes nothing (its peers' receive waits then run out as well).
+    // Split-K across a cluster. The two consumer groups first add up in shared memory (the weight
+    // ring is free once both are past their last stage), then every warp of the first group pushes
+    // its live groups of four partial sums into the receive buffer of the rank that adds them, at the
+    // slot of its own rank; no cluster barrier and no remote load sits between the last product and
+    // the sums. A CTA that gave up a wait pushes nothing (its peers' receive waits then run out).
     const bool aborted = ld_flag(abort_flag) != 0u;
-    if (warp < kConsumers && !aborted) {
-      const int slot = rank * NCG + warp / kBlocksPerRow;
+    const int cw = warp % kBlocksPerRow;
+    if constexpr (NCG == 2) {
+      float4 *gred = reinterpret_cast<float4 *>(base_ptr + L::kOffP);
+      if (warp < kConsumers) asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+      if (warp >= kBlocksPerRow && warp < kConsumers) {
+#pragma unroll
+        for (int jt = 0; jt < J; ++jt)
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            gred[((cw * 2 + q) * J + jt) * 32 + lane] = make_float4(acc[jt][q][0], acc[jt][q][1], acc[jt][q][2], acc[jt][q][3]);
+      }
+      if (warp < kConsumers) asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+      if (warp < kBlocksPerRow) {
+#pragma unroll
+        for (int jt = 0; jt < J; ++jt)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const float4 v = gred[((cw * 2 + q) * J + jt) * 32 + lane];
+            acc[jt][q][0] += v.x;
+            acc[jt][q][1] += v.y;
+            acc[jt][q][2] += v.z;
+            acc[jt][q][3] += v.w;
+          }
+      }
+    }
+    if (warp < kBlocksPerRow && !aborted) {
       const uint32_t recv0 = base + L::kOffRecv;
 #pragma unroll
       for (int jt = 0; jt < J; ++jt)
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int m = 8 * jt + 2 * tig + (e & 1);
-            if (m < rows) {
-              const int o = m * BN + nl0 + q + 2 * (e >> 1);
-              const int dst = o / per;
-              const uint32_t a = recv0 + 4u * uint32_t(slot * per + (o - dst * per));
-              st_async_f32(map_to_rank(a, dst), acc[jt][q][e], map_to_rank(recv_bar, dst));
-            }
+        for (int q = 0; q < 2; ++q) {
+          if (8 * jt + 2 * tig < rows) {
+            const int g = ((cw * 2 + q) * J + jt) * 32 + lane;
+            const int dst = g / per_g;
+            const uint32_t a = recv0 + 16u * uint32_t(rank * per_g + (g - dst * per_g));
+            st_async_v4(map_to_rank(a, dst), acc[jt][q][0], acc[jt][q][1], acc[jt][q][2], acc[jt][q][3],
+                        map_to_rank(recv_bar, dst));
           }
+        }
     }
-    if (C > 1) cluster_arrive_relaxed();
-    // this CTA's slice: wait for every contribution, add them in (rank, group) order, store
-    bool got = my_per == 0 || wait_phase(recv_bar, 0, abort_flag, limit_ns, &g_decode_error);
+    cluster_arrive_relaxed();
+    // this CTA's slice: wait for every rank's contribution, add them in rank order, store
+    bool got = my_live == 0 || wait_phase(recv_bar, 0, abort_flag, limit_ns, &g_decode_error);
     if (got) {
-      const float *recv = reinterpret_cast<const float *>(base_ptr + L::kOffRecv);
-      for (int i = threadIdx.x; i < my_per; i += kThreads) {
-        float v = 0.f;
-        for (int sl = 0; sl < C * NCG; ++sl) v += recv[sl * per + i];
-        const int o = rank * per + i;
-        finish(o / BN, n0 + (o % BN), v);
+      const float4 *recv = reinterpret_cast<const float4 *>(base_ptr + L::kOffRecv);
+      for (int i = threadIdx.x; i < my_hi - my_lo; i += kThreads) {
+        const int g = my_lo + i;
+        const int ln = g % 32, rest = g / 32;
+        const int jt = rest % J, q = (rest / J) % 2, w = rest / (2 * J);
+        const int m0 = 8 * jt + 2 * (ln & 3);
+        if (m0 >= rows) continue;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r = 0; r < C; ++r) {
+          const float4 x = recv[r * per_g + i];
+          v[0] += x.x;
+          v[1] += x.y;
+          v[2] += x.z;
+          v[3] += x.w;
+        }
+        const int64_t n = n0 + 32 * w + 4 * (ln >> 2) + q;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) finish(m0 + (e & 1), n + 2 * (e >> 1), v[e]);
       }
     }
     // no CTA leaves while a peer may still push into its receive buffer
-    if (C > 1) cluster_wait();
+    cluster_wait();
   }
 }
 
@@ -584,64 +666,17 @@ bool decode_supported_impl(const GemmArgs &g) {
          aligned16(g.scales) && (g.qzeros == nullptr || aligned16(g.qzeros));
 }
 
-// CTAs of one decode kernel that can be resident at once when launched in clusters of C
-// (0 when unknown: no device). Queried from the runtime once per device, variant and cluster size.
-int64_t resident_ctas(int J, int C, int ncg) {
-  static std::mutex mu;
-  static int cache[64][2][2][kMaxCluster + 1];
-  static bool have[64][2][2][kMaxCluster + 1] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!have[dev][J - 1][ncg - 1][C]) {
-    const KernelFn fn = pick(W4A16_F16, J, true, false, 1, ncg);  // occupancy does not depend on the stage size
-    const int smem = smem_of(J, ncg);
-    const int threads = threads_of(ncg);
-    int n = 0;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
-        (C <= 8 || cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess)) {
-      if (C == 1) {
-        int per_sm = 0, sms = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) == cudaSuccess &&
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-          n = per_sm * sms;
-      } else {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(C), 1, 1);
-        cfg.blockDim = dim3(threads, 1, 1);
-        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = static_cast<unsigned>(C);
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess) n = clusters * C;
-      }
-    }
-    cudaGetLastError();  // a failed query leaves no sticky state
-    cache[dev][J - 1][ncg - 1][C] = n;
-    have[dev][J - 1][ncg - 1][C] = true;
-  }
-  return cache[dev][J - 1][ncg - 1][C];
-}
-
-#ifdef W4A16_PROBE
-// Tuning builds only: force the consumer-group count, the split-K factor and the stage size.
-int g_probe_ncg = 0, g_probe_c = 0, g_probe_sb = 0;
-#endif
+// Test and tuning override of the decode plan (w4a16_debug_decode_override): consumer groups,
+// split-K factor and K blocks per stage; 0 leaves the dispatcher's choice.
+std::atomic<int> g_ovr_ncg{0}, g_ovr_c{0}, g_ovr_sb{0};
 
 }  // namespace
 
-#ifdef W4A16_PROBE
-extern "C" void w4a16_probe_decode_force(int ncg, int c, int sb) {
-  g_probe_ncg = ncg;
-  g_probe_c = c;
-  g_probe_sb = sb;
+void decode_set_override(int ncg, int c, int sb) {
+  g_ovr_ncg.store(ncg, std::memory_order_relaxed);
+  g_ovr_c.store(c, std::memory_order_relaxed);
+  g_ovr_sb.store(sb, std::memory_order_relaxed);
 }
-#endif
 
 // Pipeline shape for a cluster rank holding `kb` K blocks: blocks per stage (bigger TMA boxes move
 // data faster, but a CTA with few blocks needs small stages to start early), and the rank's range
@@ -658,43 +693,45 @@ static void rank_shape(int64_t kbt, int C, int *sb, int64_t *kb_per_cta, int for
 void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool query_device,
                       w4a16_plan_t *p) {
   (void)group_size;
+  (void)query_device;
   const int J = M <= 8 ? 1 : 2;
   const int64_t n_tiles = (N + BN - 1) / BN;
   const int64_t kbt = (K + BK - 1) / BK;
-  // Choose the cluster size C (split-K factor) minimising waves x per-CTA time, where a CTA costs a
-  // fixed latency (launch, first TMA round trip, cluster reduction) plus its K blocks; the number of
-  // CTAs resident at once comes from the runtime's occupancy query (one per SM when unknown).
-  constexpr double kFixedUs = 2.5, kPerBlockUs = 0.2;
-  int ncg = 2;
+  const double sms = double(num_sms > 0 ? num_sms : 1);
+  // One consumer group per CTA (a CTA takes under half an SM, so a CTA of the next call can be
+  // resident beside it and fetch its weights before this call ends) and one K block per stage. The
+  // cluster size C (split-K factor) minimises a cost fitted to per-call times measured on GB300 for
+  // the workload layers (CUDA-graph chains of calls on rotating weight replicas, C = 1..16, M = 1 and
+  // 8): microseconds ~ 0.16 C + 0.47 kb waves + 0.53 kb over, with kb the K blocks per rank, waves
+  // the rounds of two CTAs per SM the grid needs, and over the grid's excess over one CTA per SM (in
+  // SMs): ranks that share an SM with another rank of the same call slow down, and they leave the
+  // next call no room to start early. Every rank keeps at least two K blocks.
+  int ncg = 1;
   int bestC = 1, bestSB = 1;
   double best = -1.0;
   for (int Ct = 1; Ct <= kMaxCluster; ++Ct) {
     int sb = 1;
     int64_t kb = kbt;
-    rank_shape(kbt, Ct, &sb, &kb);
+    rank_shape(kbt, Ct, &sb, &kb, 1);
     const int C = static_cast<int>((kbt + kb - 1) / kb);  // ranks left after rounding to whole stages
     if (C != Ct) continue;                                 // the same plan as a smaller C
-    if (C > 1 && kb < 2) break;                            // every rank keeps at least two K blocks
-    int64_t slots = query_device ? resident_ctas(J, C, ncg) : 0;
-    if (slots <= 0) slots = C <= 8 ? int64_t(num_sms) / C * C : 0;
-    if (slots <= 0) continue;
-    const int64_t ctas = n_tiles * C;
-    const int64_t waves = (ctas + slots - 1) / slots;
-    const double cost = double(waves) * (kFixedUs + kPerBlockUs * double(kb));
+    if (C > 1 && kb < 2) break;
+    const double grid = double(n_tiles * C);
+    const double waves = std::ceil(grid / (2.0 * sms));
+    const double over = std::max(0.0, grid - sms) / sms;
+    const double cost = 0.16 * C + 0.47 * double(kb) * waves + 0.53 * double(kb) * over;
     if (best < 0 || cost < best - 1e-9) {
       best = cost;
       bestC = C;
       bestSB = sb;
     }
   }
-#ifdef W4A16_PROBE
-  if (g_probe_ncg) ncg = g_probe_ncg;
-  if (g_probe_c) {
+  if (const int o = g_ovr_ncg.load(std::memory_order_relaxed)) ncg = o;
+  if (const int oc = g_ovr_c.load(std::memory_order_relaxed)) {
     int64_t kb = kbt;
-    rank_shape(kbt, g_probe_c, &bestSB, &kb, g_probe_sb);
+    rank_shape(kbt, oc, &bestSB, &kb, g_ovr_sb.load(std::memory_order_relaxed));
     bestC = static_cast<int>((kbt + kb - 1) / kb);
   }
-#endif
   p->path = W4A16_PATH_DECODE;
   p->k_blocks_per_stage = bestSB;
   p->m_tile = 8 * J;

@@ -247,17 +247,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                               : unit_begin(int64_t(blockIdx.x) + 1, total, G);
   const int n_units = dp_units + static_cast<int>(u_end - u_begin);
   const int kb_first = static_cast<int>(u_begin % nk);
-  // Tile and K block of this CTA's unit i.
-  auto unit_at = [&](int i, int64_t &t, int &kb) {
-    if (i < dp_units) {
-      t = int64_t(blockIdx.x) + int64_t(i / nk) * G;
-      kb = i % nk;
-    } else {
-      const int64_t u = u_begin + (i - dp_units);
-      t = dp_tiles + u / nk;
-      kb = static_cast<int>(u % nk);
-    }
-  };
   // The share's last segment needs a fix-up when it starts a tile (K block 0) but ends inside it: the
   // CTAs after this one hold the rest of that tile and publish their partial tiles.
   const int64_t s_first = u_begin / nk;  // first and last shared tile, counted from dp_tiles
@@ -268,6 +257,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (fix_needed)
     while (c_fix + 1 < G && unit_begin(c_fix + 1, total, G) < (s_last + 1) * nk) ++c_fix;
   const int n_con = static_cast<int>(c_fix - blockIdx.x);  // contributors to add
+  // Tile and K block of this CTA's units, walked in order by every role (no division per unit: the
+  // single MMA-issuing and producer threads are on the critical path): start at unit 0, then step.
+  struct Cursor {
+    int64_t t;
+    int kb;
+  };
+  const Cursor cur0 = dp_units > 0 ? Cursor{int64_t(blockIdx.x), 0} : Cursor{dp_tiles + s_first, kb_first};
+  auto step = [&](Cursor &c, int i_next) {  // from unit i_next - 1 to unit i_next
+    if (i_next == dp_units) {
+      c = Cursor{dp_tiles + s_first, kb_first};  // the data-parallel tiles are done: the shared ones
+    } else if (++c.kb == nk) {
+      c.kb = 0;
+      c.t += i_next < dp_units ? G : 1;
+    }
+  };
 
   const uint32_t bar0 = base + kOffBar;
   auto full_a = [&](int s) { return bar0 + 8u * s; };
@@ -353,23 +357,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // other ring in steady state, and every wait depends only on work already requested.
       constexpr int kLag = kShared ? 0 : SP - SA;
       int issued_p = 0, issued_a = 0;
-      auto issue_a = [&](int j) -> bool {
+      Cursor cp = cur0, ca = cur0;
+      auto issue_a = [&](int j) -> bool {  // units in order: j == issued_a
         const int s = j % SA;
         if (!wait_phase(empty_a(s), ((j / SA) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error)) return false;
-        int64_t ta;
-        int kba;
-        unit_at(j, ta, kba);
+        if (j > 0) step(ca, j);
         mbar_arrive_expect_tx(full_a(s), tx_a);
-        tma_load_2d(base + kOffA + s * kABytes, &tmA, kba * BK, static_cast<int>((ta % p.m_tiles) * BM), full_a(s));
+        tma_load_2d(base + kOffA + s * kABytes, &tmA, ca.kb * BK, static_cast<int>((ca.t % p.m_tiles) * BM), full_a(s));
         issued_a = j + 1;
         return true;
       };
       bool run = true;
       for (int j = 0; j < n_units && run; ++j) {
         const int s = j % SP;
-        int64_t tp;
-        int kbp;
-        unit_at(j, tp, kbp);
+        if (j > 0) step(cp, j);
+        const int64_t tp = cp.t;
+        const int kbp = cp.kb;
         run = wait_phase(empty_p(s), ((j / SP) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error);
         if (!run) break;
         if constexpr (kShared) {
@@ -446,11 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int seg = 0;
       bool seg_start = true;
+      Cursor cm = cur0;
       for (int i = 0; i < n_units && ok; ++i) {
         const int sa = i % SA, sb = i % SB;
-        int64_t ti;
-        int kb;
-        unit_at(i, ti, kb);
+        if (i > 0) step(cm, i);
+        const int kb = cm.kb;
         if (seg_start && seg > 0) {
           // the epilogue of the previous segment has read the accumulators out of TMEM
           ok = wait_phase(accum_empty, (seg - 1) & 1, abort_flag, limit_ns, &g_prefill_error);
@@ -519,10 +522,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int seg = 0, seg_kb0 = 0, epi_uses = 0;
     bool seg_open = false;  // a segment (one tile's run of K blocks) has started
     const int dgrp = dw / kGroupWarps, dwg = dw % kGroupWarps;  // dequantiser group, warp within it
+    Cursor ce = cur0;
     for (int i = 0; i < n_units && ok; ++i) {
-      int64_t t;
-      int kb;
-      unit_at(i, t, kb);
+      if (i > 0) step(ce, i);
+      const int64_t t = ce.t;
+      const int kb = ce.kb;
       if (!seg_open) {
         seg_kb0 = kb;  // K block the segment starts at: 0 unless a share starts inside the tile
         seg_open = true;

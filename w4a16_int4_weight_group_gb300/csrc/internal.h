@@ -74,6 +74,10 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
 bool decode_weight_maps(const GemmArgs &g, const w4a16_plan_t &p, WeightMaps *wm);
 // wm: weight descriptors encoded for this plan, or null (encoded per call).
 cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &p, const WeightMaps *wm = nullptr);
+// Override of the decode plan's consumer groups, split-K factor and stage size (0: automatic).
+void decode_set_override(int ncg, int c, int sb);
+// Changes whenever a debug setting that alters plans changes (cached plans are dropped then).
+uint64_t plan_epoch();
 cudaError_t decode_take_device_error(uint32_t *err);
 cudaError_t decode_set_wait_limit_ns(uint64_t ns);
 cudaError_t decode_set_stall(bool on);
