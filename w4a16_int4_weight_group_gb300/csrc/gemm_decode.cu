@@ -121,7 +121,7 @@ struct DecodeParams {
   int kb_total;     // K blocks of the problem
   int srows;        // scale / zero-point rows per stage
   int g_shift;      // log2(G) when a stage spans several scale groups, else 31 (one group per stage)
-  int bpg;          // K blocks per scale group for G in {64, 128}; 0 when a group outlasts every stage
+  int bpg;          // K blocks per scale group (1 or 2) for G in {64, 128}; 0 when a group outlasts every stage
 };
 
 // A 16-bit float (fp16 or bf16 bits) widened exactly to fp32.
@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(threads_of(NCG), NCG == 1 ? 2 : W4A16_DEC_MINB
             // end of a scale group: every segment for G = 32; for larger G the block whose end is
             // a multiple of G; and always the stage's last block
             const int kend = kb_begin + js * SB + b + 1;  // K blocks done after this one
-            if (TWO_GROUPS || b == nb - 1 || (p.bpg > 0 && kend % p.bpg == 0)) flush(sraw[g], zraw[g]);
+            if (TWO_GROUPS || b == nb - 1 || (p.bpg > 0 && (kend & (p.bpg - 1)) == 0)) flush(sraw[g], zraw[g]);
           }
         }
       }
