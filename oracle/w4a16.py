@@ -90,6 +90,52 @@ def unpack_k(k_packed: np.ndarray) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------------------------
+# prepacked weight layout (this library's kernel-native layout; the pages' kernels read b_q as is)
+# ----------------------------------------------------------------------------------------------
+# The packed words b_q[K, N/8] regrouped into blocks of 64 rows x 32 words (a 64-row K block of a
+# 256-column tile), blocks ordered tile-major then K block, each block contiguous (8 KB); K and N are
+# padded with zero words to multiples of 64 and 256. Inside a block, row r occupies 32 consecutive
+# words, and its 16-byte chunks (four words each) are permuted by XOR with r mod 8: word w of row r
+# sits at position 4 * ((w // 4) ^ (r % 8)) + w % 4 of the row. (That is where a 2-D copy with a
+# 128-byte swizzle places the same 64 x 128-byte box.)
+PP_ROWS, PP_WORDS = 64, 32
+
+
+def prepack(b_q: np.ndarray) -> np.ndarray:
+    """int32 [K, N/8] -> int32 [ceil(N/256), ceil(K/64), 64, 32] in the prepacked layout."""
+    b_q = np.asarray(b_q).view(np.int32)
+    K, NW = b_q.shape
+    tiles, kbs = -(-NW // PP_WORDS), -(-K // PP_ROWS)
+    out = np.zeros((tiles, kbs, PP_ROWS, PP_WORDS), dtype=np.int32)
+    for t in range(tiles):
+        for kb in range(kbs):
+            for r in range(PP_ROWS):
+                k = kb * PP_ROWS + r
+                if k >= K:
+                    continue
+                for w in range(PP_WORDS):
+                    c = t * PP_WORDS + w
+                    if c >= NW:
+                        continue
+                    pos = 4 * ((w // 4) ^ (r % 8)) + w % 4
+                    out[t, kb, r, pos] = b_q[k, c]
+    return out
+
+
+def unprepack(b_pp: np.ndarray, k: int, n: int) -> np.ndarray:
+    """The inverse of ``prepack`` for a [k, n] weight matrix: int32 [k, n/8]."""
+    b_pp = np.asarray(b_pp).view(np.int32)
+    nw = n // 8
+    out = np.zeros((k, nw), dtype=np.int32)
+    for kk in range(k):
+        kb, r = divmod(kk, PP_ROWS)
+        for c in range(nw):
+            t, w = divmod(c, PP_WORDS)
+            out[kk, c] = b_pp[t, kb, r, 4 * ((w // 4) ^ (r % 8)) + w % 4]
+    return out
+
+
+# ----------------------------------------------------------------------------------------------
 # dequantisation
 # ----------------------------------------------------------------------------------------------
 def zero_points(qzeros: Optional[np.ndarray], zp_bias: int, n_groups: int, cols) -> np.ndarray:
@@ -185,6 +231,6 @@ def fp64_eps_bound(K: int) -> float:
     return 1e-12 * max(1, K)
 
 
-__all__ = ["pack", "unpack", "pack_k", "unpack_k", "zero_points", "dequant_exact", "dequant_t", "gemm_ref",
+__all__ = ["pack", "unpack", "pack_k", "unpack_k", "prepack", "unprepack", "zero_points", "dequant_exact", "dequant_t", "gemm_ref",
            "weight_rounding_bound", "out_t", "tolerance", "within_tolerance", "TOLERANCE",
            "SUPPORTED_GROUP_SIZES", "t_unit_roundoff", "t_min_subnormal"]

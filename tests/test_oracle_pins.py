@@ -474,3 +474,36 @@ def test_pack_k_round_trip_and_relation_to_n_packing():
     assert np.array_equal(oracle.unpack(oracle.pack(q)), oracle.unpack_k(kp))
     # the layouts really differ: the first K-packed word holds column 0, rows 0..7
     assert int(kp.view(np.uint32)[0, 0]) == sum(int(q[k, 0]) << (4 * k) for k in range(8))
+
+
+def test_prepack_hand_derived_positions():
+    """The prepacked layout: each hand-derived position (tests/golden/prepack_words.json) holds the
+    word it should, the padding is zero, and the layout has exactly the words it should."""
+    g = _golden("prepack_words.json")
+    K, N = g["K"], g["N"]
+    kk, cc = np.meshgrid(np.arange(K), np.arange(N // 8), indexing="ij")
+    b_q = (1000 * kk + cc + 1).astype(np.int32)
+    pp = oracle.prepack(b_q)
+    assert list(pp.shape) == g["shape"]
+    flat = pp.reshape(-1)
+    for e in g["entries"]:
+        assert flat[e["flat"]] == 1000 * e["k"] + e["c"] + 1, e["why"]
+    for z in g["zeros"]:
+        assert flat[z["flat"]] == 0, z["why"]
+    assert int((flat == 0).sum()) == g["zero_words_total"]
+
+
+def test_prepack_round_trip_and_block_contents():
+    """unprepack(prepack(b)) == b on shapes with ragged K and N tails, and every 64-row block of a
+    tile holds exactly the words of those rows and columns (as a set), whatever their order."""
+    rng = np.random.default_rng(7)
+    for K, N in ((64, 256), (130, 264), (200, 1000), (1, 8)):
+        b = rng.integers(1, 2 ** 31, size=(K, N // 8), dtype=np.int64).astype(np.int32)
+        pp = oracle.prepack(b)
+        assert np.array_equal(oracle.unprepack(pp, K, N), b)
+        for t in range(pp.shape[0]):
+            for kb in range(pp.shape[1]):
+                block = pp[t, kb]
+                want = b[kb * 64:(kb + 1) * 64, t * 32:(t + 1) * 32]
+                for r in range(want.shape[0]):
+                    assert sorted(block[r][block[r] != 0].tolist()) == sorted(want[r].tolist())
