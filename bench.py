@@ -60,6 +60,7 @@ SUSTAINED_AFTER_S = 1.0
 
 WORKLOADS = {
     "decode": "decode M<=8: decode_2112 cases then decode_4b cases (19 calls per step)",
+    "decode_pp": "the decode workload with the weights in the library's prepacked layout (w4a16_prepack)",
     "decode_2112": "decode, non-Marlin-aligned: M in {1,2,4,5,8} x (K,N) in {(1152,4224),(2112,1152)}, "
                    "G=32, bf16, symmetric uint4b8, scales U[0.005,0.02], A~N(0,1)",
     "decode_4b": "decode 4B-class: M in {1,4,8} x (K,N) in {(2560,3840),(2560,19456),(9728,2560)}, G=128, "
@@ -73,7 +74,7 @@ WORKLOADS = {
     "tiny": "tiny: M=4, K=256, N=512, G=128, fp16, symmetric",
 }
 # the workloads the default run reports beside the headline
-SIDE_WORKLOADS = ["decode_2112", "decode_4b", "mid_m", "prefill", "sweep"]
+SIDE_WORKLOADS = ["decode_2112", "decode_4b", "decode_pp", "mid_m", "prefill", "sweep"]
 
 
 def log(*a):
@@ -98,7 +99,7 @@ def sweep_sample():
 
 
 def cases_of(name):
-    if name == "decode":
+    if name in ("decode", "decode_pp"):
         return list(synth.config_cases("decode_2112")) + list(synth.config_cases("decode_4b"))
     if name == "sweep":
         return sweep_sample()
@@ -312,7 +313,11 @@ class Workload:
             scs = [sc] + [sc.clone() for _ in range(reps - 1)]
             qzs = None if qz is None else [qz] + [qz.clone() for _ in range(reps - 1)]
             # one prepared layer per weight replica (the public API a model would hold per layer)
-            layers = [w4.W4A16Linear(b_qs[r], scs[r], None if qzs is None else qzs[r], G, 8, bi) for r in range(reps)]
+            pp = name.endswith("_pp")
+            layers = [w4.W4A16Linear(b_qs[r], scs[r], None if qzs is None else qzs[r], G, 8, bi, prepacked=pp)
+                      for r in range(reps)]
+            if pp:  # the prepacked layers keep their own copies; the canonical replicas are not needed
+                b_qs = None
             self.pools[key] = {"layers": layers, "reps": reps, "keep": (b_qs, scs, qzs, bi)}
         # activations and outputs of all the calls of a step: one device buffer per dtype (16-byte
         # aligned slices), mirrored by pinned host buffers; the end-to-end leg moves a step's inputs

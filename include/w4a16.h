@@ -117,6 +117,25 @@ w4a16_status w4a16_repack_k_to_n(const int32_t *k_packed, int32_t *b_q, int64_t 
                                  w4a16_stream_t stream);
 
 /*
+ * Prepacked weights: this library's kernel-native layout of b_q (a load-time step; the pages' kernels
+ * read b_q as it is). The packed words are regrouped into blocks of 64 K rows x 32 words (the 256
+ * output columns of one column tile), stored tile-major and then by K block, each block 8 KB
+ * contiguous; K and N are padded with zero words to multiples of 64 and 256. Inside a block row r
+ * holds its 32 words with the 16-byte chunk j at position j ^ (r % 8) - the order in which the
+ * kernels keep a block in shared memory - so a block reaches shared memory by one plain bulk copy
+ * instead of a 64-row tensor copy. Both the decode and the prefill kernels read it; the generic path
+ * does not.
+ *
+ * w4a16_prepack_bytes - bytes of the prepacked form of a [k, n] weight matrix (0 for invalid sizes).
+ * w4a16_prepack - b_q int32 [k, n/8] -> b_pp (w4a16_prepack_bytes(k, n) bytes, 16-byte aligned), every
+ *   byte written (padding included). Device pointers, stream-ordered, no allocation.
+ *   Errors: INVALID_ARG (k or n not positive, n % 8 != 0, NULL, overlap), MISALIGNED (b_q 4 bytes,
+ *   b_pp 16 bytes).
+ */
+size_t w4a16_prepack_bytes(int64_t k, int64_t n);
+w4a16_status w4a16_prepack(const int32_t *b_q, int32_t *b_pp, int64_t k, int64_t n, w4a16_stream_t stream);
+
+/*
  * w4a16_dequant - materialise dequant(W) in the activation dtype:
  *   w_out[k, n] = RNE_dtype((q[k, n] - zp[k/G, n]) * scales[k/G, n])
  * i.e. the exact product rounded once to nearest-even (dequantisation rule: PR #40977 report, key
@@ -223,6 +242,16 @@ typedef struct w4a16_layer_st *w4a16_layer_t;
 w4a16_status w4a16_layer_create(const int32_t *b_q, const void *scales, const int32_t *qzeros, int group_size,
                                 int zp_bias, const void *bias, int64_t k, int64_t n, w4a16_dtype dtype,
                                 w4a16_layer_t *layer);
+/*
+ * w4a16_layer_create_prepacked - as w4a16_layer_create, with the weights in the prepacked layout
+ *   (b_pp from w4a16_prepack, 16-byte aligned) instead of b_q. Its calls produce exactly the results of
+ *   a layer built on b_q. They run on the TMA-fed kernels only: a call that would take the generic
+ *   path (a or out not 16-byte aligned, n % 32 != 0, k % 8 != 0, or a forced generic path) returns
+ *   W4A16_ERR_UNSUPPORTED.
+ */
+w4a16_status w4a16_layer_create_prepacked(const int32_t *b_pp, const void *scales, const int32_t *qzeros,
+                                          int group_size, int zp_bias, const void *bias, int64_t k, int64_t n,
+                                          w4a16_dtype dtype, w4a16_layer_t *layer);
 w4a16_status w4a16_layer_gemm(w4a16_layer_t layer, const void *a, void *out, int64_t m, void *workspace,
                               size_t workspace_bytes, w4a16_stream_t stream);
 size_t w4a16_layer_workspace_size(w4a16_layer_t layer, int64_t m);

@@ -211,24 +211,23 @@ def test_force_path_entry_point_validates(w):
 
 # Decode plans the dispatcher picks on a 152-SM GB300 for the decode workloads' layers, against the
 # plans that measured fastest there (per-call time of CUDA-graph chains of calls over rotating weight
-# replicas, every split-K factor 1..16 tried with one and two consumer groups and stages of one and
-# two K blocks; M = 1 and M = 8): one consumer group (9 warps), one K block per stage, and this
-# split-K factor.
-MEASURED_BEST_DECODE_SPLIT = {
-    (1152, 4224, 32): 6,     # 102 CTAs, 2.8 us
-    (2112, 1152, 32): 11,    # 55 CTAs, 2.7-2.9 us
-    (2560, 3840, 128): 10,   # 150 CTAs, 4.2-4.4 us
-    (2560, 19456, 128): 2,   # 152 CTAs, 8.8-9.1 us
-    (9728, 2560, 128): 14,   # 140 CTAs
+# replicas; split-K factors 1..16, one and two consumer groups, stages of one, two and four K blocks;
+# M = 1 and M = 8): one consumer group (9 warps) and this (split-K factor, K blocks per stage).
+MEASURED_BEST_DECODE_PLAN = {
+    (1152, 4224, 32): (6, 1),     # 102 CTAs, 2.8 us
+    (2112, 1152, 32): (11, 1),    # 55 CTAs, 2.7-2.9 us
+    (2560, 3840, 128): (10, 2),   # 150 CTAs, 4.1-4.3 us
+    (2560, 19456, 128): (2, 2),   # 152 CTAs, 8.3-8.5 us
+    (9728, 2560, 128): (16, 2),   # 160 CTAs, 6.8-7.0 us
 }
 
 
-@pytest.mark.parametrize("shape", sorted(MEASURED_BEST_DECODE_SPLIT))
+@pytest.mark.parametrize("shape", sorted(MEASURED_BEST_DECODE_PLAN))
 def test_decode_planner_picks_the_measured_best_plan(w, shape):
     K, N, G = shape
     for M in (1, 2, 4, 5, 8):
         for dt, zp in ((0, True), (1, False)):
             p = w.w4a16_plan(M, K, N, G, dt, zp, 152, False)
             assert p["path_name"] == "decode"
-            assert (p["warps"], p["k_split"], p["k_blocks_per_stage"]) == (9, MEASURED_BEST_DECODE_SPLIT[shape], 1), p
+            assert (p["warps"], p["k_split"], p["k_blocks_per_stage"]) == (9, *MEASURED_BEST_DECODE_PLAN[shape]), p
             assert p["grid"] == -(-N // 256) * p["k_split"]

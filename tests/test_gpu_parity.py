@@ -442,3 +442,58 @@ def test_every_decode_configuration_matches_oracle(w, M, K, N, G, dt, asym, bias
     finally:
         w.w4a16_debug_decode_override(0, 0, 0)
     assert w.w4a16_get_device_error() == 0
+
+
+@pytest.mark.parametrize("K,N", [(64, 256), (130, 264), (2112, 1152), (2560, 3840), (4104, 288)])
+def test_prepack_bitexact(w, K, N):
+    """w4a16_prepack on the GPU writes exactly the oracle's prepacked layout, padding included."""
+    rng = np.random.default_rng(K + N)
+    b = rng.integers(0, 2 ** 32, size=(K, N // 8), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    got = w.w4a16_prepack(torch.from_numpy(b).cuda())
+    torch.cuda.synchronize()
+    want = oracle.prepack(b).reshape(-1)
+    assert got.numel() == want.size == w.lib().w4a16_prepack_bytes(K, N) // 4
+    assert np.array_equal(got.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("M,K,N,G,dt,asym,bias", [(1, 1152, 4224, 32, "bf16", False, False),
+                                                 (8, 2560, 3840, 128, "f16", True, True),
+                                                 (5, 4104, 288, 4104, "bf16", True, False),
+                                                 (40, 5120, 1024, 128, "f16", False, True),
+                                                 (300, 2048, 768, 64, "bf16", True, True),
+                                                 (1024, 4096, 1024, 32, "f16", True, False)])
+def test_prepacked_layer_equals_the_canonical_one(w, M, K, N, G, dt, asym, bias):
+    """A layer on the prepacked weights gives exactly the bits of the layer on b_q (decode, mid-M
+    cluster split, prefill with stream-K; ragged K and N), and passes the oracle on its path's
+    reading; on the decode path every configuration, and identity-A, as well."""
+    c = synth.make_case(M, K, N, G, dt, asym=asym, bias=bias, seed=M + K + 1)
+    t = case_tensors(c)
+    canon = w.W4A16Linear(t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"])
+    pp = w.W4A16Linear(t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"], prepacked=True)
+    want, got = canon(t["a"]), pp(t["a"])
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    rng = np.random.default_rng(M)
+    rows = sorted({0, M - 1} | set(rng.integers(0, M, size=4).tolist()))
+    check_against_oracle(c, torch_to_bits(got), rows=rows, cols=sample_cols(N, rng, k=64), label="prepacked",
+                         path=path_taken(w, c))
+    if path_taken(w, c) == "decode":
+        try:
+            for ncg, C, sb in DECODE_VARIANTS:
+                w.w4a16_debug_decode_override(ncg, C, sb)
+                a, b = canon(t["a"]), pp(t["a"])
+                torch.cuda.synchronize()
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (ncg, C, sb)
+        finally:
+            w.w4a16_debug_decode_override(0, 0, 0)
+
+
+def test_prepacked_layer_refuses_the_generic_path(w):
+    c = synth.make_case(4, 512, 1024, 128, "f16", seed=5)
+    t = case_tensors(c)
+    pp = w.W4A16Linear(t["b_q"], t["scales"], None, 128, 8, None, prepacked=True)
+    a2 = torch.empty(c.M * c.K + 1, dtype=torch.float16, device="cuda")[1:].view(c.M, c.K)
+    a2.copy_(t["a"])
+    with pytest.raises(w.W4A16Error) as e:
+        pp(a2)
+    assert e.value.status == 2

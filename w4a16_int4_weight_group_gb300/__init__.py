@@ -57,6 +57,10 @@ SIGNATURES = [
     ("w4a16_gemm_workspace_size", ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_int, _c_int]),
     ("w4a16_layer_create", _c_int, [_vp, _vp, _vp, _c_int, _c_int, _vp, _c_i64, _c_i64, _c_int,
                                     ctypes.POINTER(_vp)]),
+    ("w4a16_layer_create_prepacked", _c_int, [_vp, _vp, _vp, _c_int, _c_int, _vp, _c_i64, _c_i64, _c_int,
+                                              ctypes.POINTER(_vp)]),
+    ("w4a16_prepack_bytes", ctypes.c_size_t, [_c_i64, _c_i64]),
+    ("w4a16_prepack", _c_int, [_vp, _vp, _c_i64, _c_i64, _vp]),
     ("w4a16_layer_gemm", _c_int, [_vp, _vp, _vp, _c_i64, _vp, ctypes.c_size_t, _vp]),
     ("w4a16_layer_workspace_size", ctypes.c_size_t, [_vp, _c_i64]),
     ("w4a16_layer_destroy", _c_int, [_vp]),
@@ -178,6 +182,22 @@ def w4a16_repack_k_to_n(k_packed: torch.Tensor, b_q: Optional[torch.Tensor] = No
     return b_q
 
 
+def w4a16_prepack(b_q: torch.Tensor, b_pp: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """b_q int32 [K, N/8] -> the prepacked layout (a flat int32 tensor of w4a16_prepack_bytes / 4
+    words; see the C header)."""
+    if b_q.dtype != torch.int32 or b_q.dim() != 2:
+        raise ValueError("b_q must be a 2-D int32 tensor")
+    k, n = b_q.shape[0], b_q.shape[1] * 8
+    nbytes = int(lib().w4a16_prepack_bytes(k, n))
+    if b_pp is None:
+        b_pp = torch.empty(nbytes // 4, dtype=torch.int32, device=b_q.device)
+    if b_pp.numel() * 4 < nbytes:
+        raise ValueError(f"b_pp holds {b_pp.numel() * 4} bytes, {nbytes} needed")
+    dev = _require_cuda(b_q, b_pp)
+    _check(lib().w4a16_prepack(_ptr(b_q), _ptr(b_pp), k, n, _stream(dev)))
+    return b_pp
+
+
 def w4a16_dequant(b_q: torch.Tensor, scales: torch.Tensor, qzeros: Optional[torch.Tensor], group_size: int,
                   zp_bias: int = 8, w_out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """dequant(W)[k, n] = RNE_dtype((q - zp) * scale) as a [K, N] tensor of the scales' dtype."""
@@ -263,7 +283,10 @@ class W4A16Linear:
     """
 
     def __init__(self, b_q: torch.Tensor, scales: torch.Tensor, qzeros: Optional[torch.Tensor], group_size: int,
-                 zp_bias: int = 8, bias: Optional[torch.Tensor] = None, use_workspace: bool = True):
+                 zp_bias: int = 8, bias: Optional[torch.Tensor] = None, use_workspace: bool = True,
+                 prepacked: bool = False):
+        """prepacked: keep the weights in the library's prepacked layout (w4a16_prepack, made here
+        from b_q on the current stream) and run the layer on it; b_q is not kept."""
         if b_q.dim() != 2 or b_q.dtype != torch.int32:
             raise ValueError("b_q must be a 2-D int32 tensor [K, N/8]")
         if qzeros is not None and qzeros.dtype != torch.int32:
@@ -277,14 +300,24 @@ class W4A16Linear:
         self.code = _dtype_code(scales.dtype)
         self.group_size, self.zp_bias = int(group_size), int(zp_bias)
         self.use_workspace = use_workspace
-        self._tensors = (b_q, scales, qzeros, bias)
         self._need = {}
         L = lib()
         h = ctypes.c_void_p()
+        self.prepacked = prepacked
         with torch.cuda.device(self.device):
-            _check(L.w4a16_layer_create(b_q.data_ptr(), scales.data_ptr(), None if qzeros is None else qzeros.data_ptr(),
-                                        self.group_size, self.zp_bias, None if bias is None else bias.data_ptr(),
-                                        self.k, self.n, self.code, ctypes.byref(h)))
+            if prepacked:
+                b_pp = w4a16_prepack(b_q)
+                self._tensors = (b_pp, scales, qzeros, bias)
+                _check(L.w4a16_layer_create_prepacked(b_pp.data_ptr(), scales.data_ptr(),
+                                                      None if qzeros is None else qzeros.data_ptr(), self.group_size,
+                                                      self.zp_bias, None if bias is None else bias.data_ptr(),
+                                                      self.k, self.n, self.code, ctypes.byref(h)))
+            else:
+                self._tensors = (b_q, scales, qzeros, bias)
+                _check(L.w4a16_layer_create(b_q.data_ptr(), scales.data_ptr(),
+                                            None if qzeros is None else qzeros.data_ptr(), self.group_size,
+                                            self.zp_bias, None if bias is None else bias.data_ptr(),
+                                            self.k, self.n, self.code, ctypes.byref(h)))
         self._handle = h.value
         self._lib = L
         self._gemm = L.w4a16_layer_gemm
@@ -385,7 +418,7 @@ def w4a16_version() -> str:
     return lib().w4a16_version().decode()
 
 
-__all__ = ["w4a16_pack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_can_implement", "w4a16_plan",
+__all__ = ["w4a16_pack", "w4a16_unpack", "w4a16_prepack", "w4a16_dequant", "w4a16_gemm", "w4a16_can_implement", "w4a16_plan",
            "w4a16_gemm_workspace_size", "workspace_for",
            "w4a16_get_device_error", "w4a16_debug_selected_path", "w4a16_debug_force_path",
            "w4a16_debug_decode_override",

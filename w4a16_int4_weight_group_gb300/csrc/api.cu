@@ -331,6 +331,25 @@ w4a16_status w4a16_repack_k_to_n(const int32_t *k_packed, int32_t *b_q, int64_t 
   return ok();
 }
 
+size_t w4a16_prepack_bytes(int64_t k, int64_t n) {
+  if (k <= 0 || n <= 0 || k >= kMaxDim || n > kMaxN || n % 8) return 0;
+  return prepack_bytes(k, n);
+}
+
+w4a16_status w4a16_prepack(const int32_t *b_q, int32_t *b_pp, int64_t k, int64_t n, w4a16_stream_t stream) {
+  if (k <= 0 || n <= 0 || k >= kMaxDim || n > kMaxN)
+    return fail(W4A16_ERR_INVALID_ARG, "k (%lld) and n (%lld) must be > 0", (long long)k, (long long)n);
+  if (n % 8) return fail(W4A16_ERR_INVALID_ARG, "n (%lld) must be divisible by 8", (long long)n);
+  if (!b_q || !b_pp) return fail(W4A16_ERR_INVALID_ARG, "b_q and b_pp must not be NULL");
+  if (!aligned(b_q, 4) || !aligned(b_pp, 16))
+    return fail(W4A16_ERR_MISALIGNED, "b_q must be 4-byte and b_pp 16-byte aligned");
+  if (overlaps(range(b_q, k * n / 2), range(b_pp, static_cast<int64_t>(prepack_bytes(k, n)))))
+    return fail(W4A16_ERR_INVALID_ARG, "b_q and b_pp overlap");
+  const cudaError_t e = launch_prepack(b_q, b_pp, k, n, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "w4a16_prepack launch");
+  return ok();
+}
+
 w4a16_status w4a16_dequant(const int32_t *b_q, const void *scales, const int32_t *qzeros, int64_t k,
                            int64_t n, int group_size, int zp_bias, w4a16_dtype dtype, void *w_out,
                            w4a16_stream_t stream) {
@@ -475,18 +494,20 @@ struct w4a16_layer_st {
 
 extern "C" {
 
-w4a16_status w4a16_layer_create(const int32_t *b_q, const void *scales, const int32_t *qzeros, int group_size,
-                                int zp_bias, const void *bias, int64_t k, int64_t n, w4a16_dtype dtype,
-                                w4a16_layer_t *layer) {
+static w4a16_status layer_create(const int32_t *b_q, const int32_t *b_pp, const void *scales, const int32_t *qzeros,
+                                 int group_size, int zp_bias, const void *bias, int64_t k, int64_t n, w4a16_dtype dtype,
+                                 w4a16_layer_t *layer) {
   if (!layer) return fail(W4A16_ERR_INVALID_ARG, "layer must not be NULL");
   *layer = nullptr;
   w4a16_status st = check_config(k, n, group_size, dtype);
   if (st != W4A16_OK) return st;
   if (!qzeros && (zp_bias < 0 || zp_bias > 15))
     return fail(W4A16_ERR_INVALID_ARG, "zp_bias (%d) must be in [0, 15]", zp_bias);
-  if (!b_q || !scales) return fail(W4A16_ERR_INVALID_ARG, "b_q and scales must not be NULL");
-  if (!aligned(b_q, 4) || !aligned(scales, 2) || (qzeros && !aligned(qzeros, 4)) || (bias && !aligned(bias, 2)))
-    return fail(W4A16_ERR_MISALIGNED, "tensors must be naturally aligned (2 bytes for 16-bit, 4 for int32)");
+  if (!(b_q || b_pp) || !scales) return fail(W4A16_ERR_INVALID_ARG, "the weights and scales must not be NULL");
+  if ((b_q && !aligned(b_q, 4)) || (b_pp && !aligned(b_pp, 16)) || !aligned(scales, 2) ||
+      (qzeros && !aligned(qzeros, 4)) || (bias && !aligned(bias, 2)))
+    return fail(W4A16_ERR_MISALIGNED, "tensors must be naturally aligned (2 bytes for 16-bit, 4 for int32, 16 for "
+                "prepacked weights)");
   int dev = 0;
   const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "device query");
@@ -494,9 +515,30 @@ w4a16_status w4a16_layer_create(const int32_t *b_q, const void *scales, const in
   if (!L) return fail(W4A16_ERR_INVALID_ARG, "out of host memory");
   L->proto = GemmArgs{nullptr, b_q, scales, qzeros, group_size, zp_bias, bias, nullptr, 0, k, n,
                       static_cast<int>(dtype), nullptr};
+  L->proto.b_pp = b_pp;
   L->device = dev;
   *layer = L;
   return ok();
+}
+
+w4a16_status w4a16_layer_create(const int32_t *b_q, const void *scales, const int32_t *qzeros, int group_size,
+                                int zp_bias, const void *bias, int64_t k, int64_t n, w4a16_dtype dtype,
+                                w4a16_layer_t *layer) {
+  if (!b_q) {
+    if (layer) *layer = nullptr;
+    return fail(W4A16_ERR_INVALID_ARG, "b_q and scales must not be NULL");
+  }
+  return layer_create(b_q, nullptr, scales, qzeros, group_size, zp_bias, bias, k, n, dtype, layer);
+}
+
+w4a16_status w4a16_layer_create_prepacked(const int32_t *b_pp, const void *scales, const int32_t *qzeros,
+                                          int group_size, int zp_bias, const void *bias, int64_t k, int64_t n,
+                                          w4a16_dtype dtype, w4a16_layer_t *layer) {
+  if (!b_pp) {
+    if (layer) *layer = nullptr;
+    return fail(W4A16_ERR_INVALID_ARG, "b_pp and scales must not be NULL");
+  }
+  return layer_create(nullptr, b_pp, scales, qzeros, group_size, zp_bias, bias, k, n, dtype, layer);
 }
 
 w4a16_status w4a16_layer_destroy(w4a16_layer_t layer) {
@@ -526,13 +568,14 @@ w4a16_status w4a16_layer_gemm(w4a16_layer_t layer, const void *a, void *out, int
   if (workspace && !aligned(workspace, 256)) return fail(W4A16_ERR_MISALIGNED, "workspace must be 256-byte aligned");
   const int64_t ng = g.K / g.group_size;
   const Range o = range(out, m * g.N * 2);
-  if (overlaps(o, range(a, m * g.K * 2)) || overlaps(o, range(g.b_q, g.K * g.N / 2)) ||
+  const Range wt = g.b_pp ? range(g.b_pp, static_cast<int64_t>(prepack_bytes(g.K, g.N))) : range(g.b_q, g.K * g.N / 2);
+  if (overlaps(o, range(a, m * g.K * 2)) || overlaps(o, wt) ||
       overlaps(o, range(g.scales, ng * g.N * 2)) || (g.qzeros && overlaps(o, range(g.qzeros, ng * g.N / 2))) ||
       (g.bias && overlaps(o, range(g.bias, g.N * 2))))
     return fail(W4A16_ERR_INVALID_ARG, "out overlaps an input tensor");
   if (workspace) {
     const Range w = range(workspace, static_cast<int64_t>(workspace_bytes));
-    if (overlaps(w, o) || overlaps(w, range(a, m * g.K * 2)) || overlaps(w, range(g.b_q, g.K * g.N / 2)) ||
+    if (overlaps(w, o) || overlaps(w, range(a, m * g.K * 2)) || overlaps(w, wt) ||
         overlaps(w, range(g.scales, ng * g.N * 2)) || (g.qzeros && overlaps(w, range(g.qzeros, ng * g.N / 2))) ||
         (g.bias && overlaps(w, range(g.bias, g.N * 2))))
       return fail(W4A16_ERR_INVALID_ARG, "workspace overlaps a tensor argument");
@@ -569,6 +612,9 @@ w4a16_status w4a16_layer_gemm(w4a16_layer_t layer, const void *a, void *out, int
   // a stream-K plan whose workspace the caller did not provide in full falls back to whole tiles
   if (workspace && workspace_bytes < prefill_plan_workspace_bytes(en.plan)) en = entry_for(false);
   const WeightMaps *wm = en.have_maps ? &en.maps : nullptr;
+  if (g.b_pp && en.plan.path != W4A16_PATH_DECODE && en.plan.path != W4A16_PATH_PREFILL)
+    return fail(W4A16_ERR_UNSUPPORTED, "prepacked weights are read by the TMA-fed kernels only: a and out must be "
+                "16-byte aligned, N %% 32 == 0 and K %% 8 == 0 (and no forced generic path)");
   switch (en.plan.path) {
     case W4A16_PATH_DECODE: e = launch_gemm_decode(g, en.plan, wm); break;
     case W4A16_PATH_PREFILL: e = launch_gemm_prefill(g, en.plan, wm); break;

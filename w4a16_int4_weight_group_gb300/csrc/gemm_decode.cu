@@ -122,6 +122,8 @@ struct DecodeParams {
   int srows;        // scale / zero-point rows per stage
   int g_shift;      // log2(G) when a stage spans several scale groups, else 31 (one group per stage)
   int bpg;          // K blocks per scale group (1 or 2) for G in {64, 128}; 0 when a group outlasts every stage
+  const uint8_t *b_pp;    // prepacked weights (null: b_q through the tensor map)
+  int64_t pp_tile_bytes;  // bytes of one column tile's blocks in the prepacked layout
 };
 
 // A 16-bit float (fp16 or bf16 bits) widened exactly to fp32.
@@ -260,16 +262,25 @@ __global__ void __launch_bounds__(threads_of(NCG), NCG == 1 ? 2 : W4A16_DEC_MINB
   if (warp == kConsumers) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      // prepacked weights: a stage's blocks are one contiguous run of 8 KB blocks, copied as they are
+      // (they are stored in the order the 128-byte-swizzled tensor copy would produce)
+      const uint8_t *pp_tile = p.b_pp ? p.b_pp + int64_t(blockIdx.x / C) * p.pp_tile_bytes : nullptr;
       auto stage_tx = [&](int j) {
         const int blocks = min(SB, nkb - j * SB);
-        return static_cast<uint32_t>(SB * L::kP + blocks * L::kA + p.srows * BN * 2 +
+        return static_cast<uint32_t>((pp_tile ? blocks : SB) * L::kP + blocks * L::kA + p.srows * BN * 2 +
                                      (HAS_ZP ? p.srows * BN / 2 : 0));
       };
       auto load_weights = [&](int j, int s) {
         const uint32_t full = full0 + 8u * s;
         const int k0 = (kb_begin + j * SB) * BK;
         const int grow = k0 / p.G;
-        tma_load_2d(base + L::kOffP + s * SB * L::kP, &tmP, static_cast<int>(n0 / 8), k0, full);
+        if (pp_tile) {
+          const int blocks = min(SB, nkb - j * SB);
+          bulk_load(base + L::kOffP + s * SB * L::kP, pp_tile + int64_t(kb_begin + j * SB) * L::kP,
+                    static_cast<uint32_t>(blocks * L::kP), full);
+        } else {
+          tma_load_2d(base + L::kOffP + s * SB * L::kP, &tmP, static_cast<int>(n0 / 8), k0, full);
+        }
         tma_load_2d(base + L::kOffS + s * SB * L::kS, &tmS, static_cast<int>(n0), grow, full);
         if constexpr (HAS_ZP)
           tma_load_2d(base + L::kOffZ + s * SB * L::kZ, &tmZ, static_cast<int>(n0 / 8), grow, full);
@@ -662,7 +673,7 @@ int smem_of(int J, int ncg) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool decode_supported_impl(const GemmArgs &g) {
-  return g.M <= 16 && g.N % 32 == 0 && g.K % 8 == 0 && aligned16(g.a) && aligned16(g.b_q) &&
+  return g.M <= 16 && g.N % 32 == 0 && g.K % 8 == 0 && aligned16(g.a) && aligned16(g.b_pp ? g.b_pp : g.b_q) &&
          aligned16(g.scales) && (g.qzeros == nullptr || aligned16(g.qzeros));
 }
 
@@ -699,31 +710,37 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
   const int64_t kbt = (K + BK - 1) / BK;
   const double sms = double(num_sms > 0 ? num_sms : 1);
   // One consumer group per CTA (a CTA takes under half an SM, so a CTA of the next call can be
-  // resident beside it and fetch its weights before this call ends) and one K block per stage. The
-  // cluster size C (split-K factor) minimises a cost fitted to per-call times measured on GB300 for
-  // the workload layers (CUDA-graph chains of calls on rotating weight replicas, C = 1..16, M = 1 and
-  // 8): microseconds ~ 0.16 C + 0.47 kb waves + 0.53 kb over, with kb the K blocks per rank, waves
-  // the rounds of two CTAs per SM the grid needs, and over the grid's excess over one CTA per SM (in
-  // SMs): ranks that share an SM with another rank of the same call slow down, and they leave the
-  // next call no room to start early. Every rank keeps at least two K blocks.
+  // resident beside it and fetch its weights before this call ends). The cluster size C (split-K
+  // factor) and the stage size sb minimise a cost fitted to per-call times measured on GB300 for the
+  // workload layers (CUDA-graph chains of calls on rotating weight replicas; C = 1..16, stages of 1,
+  // 2 and 4 blocks, M = 1 and 8): microseconds ~ (0.16 C + 0.47 kb waves + 0.45 kb over) x f, with kb
+  // the K blocks per rank, waves the rounds of two CTAs per SM the grid needs, over the grid's excess
+  // over one CTA per SM (in SMs) - ranks that share an SM with a rank of the same call slow down and
+  // leave the next call no room to start early - and f = 0.88 for two-block stages on ranks of at
+  // least 8 blocks, 0.97 on ranks of 4 to 7 (a stage wait per two blocks), 1 for one-block stages.
+  // Every rank keeps at least two K blocks.
   int ncg = 1;
   int bestC = 1, bestSB = 1;
   double best = -1.0;
   for (int Ct = 1; Ct <= kMaxCluster; ++Ct) {
-    int sb = 1;
-    int64_t kb = kbt;
-    rank_shape(kbt, Ct, &sb, &kb, 1);
-    const int C = static_cast<int>((kbt + kb - 1) / kb);  // ranks left after rounding to whole stages
-    if (C != Ct) continue;                                 // the same plan as a smaller C
-    if (C > 1 && kb < 2) break;
-    const double grid = double(n_tiles * C);
-    const double waves = std::ceil(grid / (2.0 * sms));
-    const double over = std::max(0.0, grid - sms) / sms;
-    const double cost = 0.16 * C + 0.47 * double(kb) * waves + 0.53 * double(kb) * over;
-    if (best < 0 || cost < best - 1e-9) {
-      best = cost;
-      bestC = C;
-      bestSB = sb;
+    for (int sbt = 1; sbt <= 2; ++sbt) {
+      int sb = 1;
+      int64_t kb = kbt;
+      rank_shape(kbt, Ct, &sb, &kb, sbt);
+      const int C = static_cast<int>((kbt + kb - 1) / kb);  // ranks left after rounding to whole stages
+      if (C != Ct) continue;                                 // the same plan as a smaller C
+      if (C > 1 && kb < 2) continue;
+      if (sb == 2 && kb < 4) continue;
+      const double grid = double(n_tiles * C);
+      const double waves = std::ceil(grid / (2.0 * sms));
+      const double over = std::max(0.0, grid - sms) / sms;
+      const double f = sb == 2 ? (kb >= 8 ? 0.88 : 0.97) : 1.0;
+      const double cost = (0.16 * C + 0.47 * double(kb) * waves + 0.45 * double(kb) * over) * f;
+      if (best < 0 || cost < best - 1e-9) {
+        best = cost;
+        bestC = C;
+        bestSB = sb;
+      }
     }
   }
   if (const int o = g_ovr_ncg.load(std::memory_order_relaxed)) ncg = o;
@@ -749,9 +766,12 @@ bool decode_weight_maps(const GemmArgs &g, const w4a16_plan_t &pl, WeightMaps *w
   const int sb = pl.k_blocks_per_stage;
   const int srows = g.group_size < BK * sb ? BK * sb / g.group_size : 1;
   const int64_t NW = g.N / 8, ng = g.K / g.group_size;
-  if (!tma_encode_2d(&wm->tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK * sb, true) ||
-      !tma_encode_2d(&wm->tS, 2, g.scales, g.N, ng, g.N * 2, BN, srows, false))
+  if (!tma_encode_2d(&wm->tS, 2, g.scales, g.N, ng, g.N * 2, BN, srows, false)) return false;
+  if (g.b_pp) {
+    wm->tP = wm->tS;  // unused: prepacked weights travel by plain bulk copies
+  } else if (!tma_encode_2d(&wm->tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK * sb, true)) {
     return false;
+  }
   if (g.qzeros) {
     if (!tma_encode_2d(&wm->tZ, 4, g.qzeros, NW, ng, NW * 4, BN / 8, srows, false)) return false;
   } else {
@@ -818,6 +838,8 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl, const 
   // scale groups of 64 or 128 rows end on K-block boundaries; a larger group (G = K) is cut only by
   // the stage ends
   prm.bpg = (g.group_size == 64 || g.group_size == 128) ? g.group_size / BK : 0;
+  prm.b_pp = reinterpret_cast<const uint8_t *>(g.b_pp);
+  prm.pp_tile_bytes = kbt * int64_t(BK * BN / 2);
 
   const int64_t n_tiles = (g.N + BN - 1) / BN;
   cudaLaunchConfig_t cfg = {};

@@ -46,6 +46,7 @@ namespace w4a16 {
 namespace {
 
 constexpr int BN = 256, BK = 64;
+constexpr int64_t kPBytesHost = BK * (BN / 8) * 4;  // one packed 64 x 256 block
 constexpr int kDequantWarps = 8;
 constexpr int kThreads = 32 * (2 + kDequantWarps);
 
@@ -171,6 +172,8 @@ struct PrefillParams {
   int csplit;        // > 1: clusters of csplit CTAs split each tile's K blocks (128-row tiles only)
   int a_rows;        // rows of A per TMA box: BM, or M rounded up to 8 when one row tile covers M
   int dp_waves;      // stream-K: whole waves of tiles done data-parallel first (CTA c: c, c + G, ...)
+  const uint8_t *b_pp;    // prepacked weights (null: b_q through the tensor map)
+  int64_t pp_tile_bytes;  // bytes of one column tile's blocks in the prepacked layout
 };
 
 // First (tile, K block) work unit of CTA c when the tiles x nk units are split evenly over G CTAs.
@@ -386,7 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n0 = static_cast<int>((tp / p.m_tiles) * BN);
         const int k0 = kbp * BK;
         const int grow = k0 / p.G;
-        tma_load_2d(base + kOffP + s * kPBytes, &tmP, n0 / 8, k0, full_p(s));
+        if (p.b_pp)  // prepacked: the block is 8 KB of contiguous words (rows with permuted chunks)
+          bulk_load(base + kOffP + s * kPBytes, p.b_pp + (tp / p.m_tiles) * p.pp_tile_bytes + int64_t(kbp) * kPBytes,
+                    kPBytes, full_p(s));
+        else
+          tma_load_2d(base + kOffP + s * kPBytes, &tmP, n0 / 8, k0, full_p(s));
         tma_load_2d(base + kOffS + s * kSBytes, &tmS, n0, grow, full_p(s));
         if constexpr (HAS_ZP) tma_load_2d(base + kOffZ + s * kZBytes, &tmZ, n0 / 8, grow, full_p(s));
         issued_p = j + 1;
@@ -499,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ dequantisers, then epilogues
     const int dw = warp - 2;  // 0..7
     const int c = lane;       // packed word column of the tile (8 output columns)
+    const int pp_swz = p.b_pp ? 7 : 0;
     const int q = warp & 3;   // TMEM lane quarter this warp may read
     const int row = 32 * q + lane;
     const int half = dw >> 2;  // epilogue columns [128*half, 128*half + 128)
@@ -550,8 +558,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           lds128(S + gr * (BN * 2) + c * 16, sw[gr][0], sw[gr][1], sw[gr][2], sw[gr][3]);
           if constexpr (HAS_ZP) zw[gr] = lds32(Z + gr * (BN / 2) + c * 4);
         }
+        // prepacked blocks hold row r's 16-byte chunk j at j ^ (r % 8); the tensor copy leaves them in order
 #pragma unroll
-        for (int ii = 0; ii < kRows; ++ii) wq[ii] = lds32(P + (dwg + kGroupWarps * ii) * (BN / 2) + c * 4);
+        for (int ii = 0; ii < kRows; ++ii) {
+          const int r = dwg + kGroupWarps * ii;
+          wq[ii] = lds32(P + r * (BN / 2) + ((((c >> 2) ^ (r & pp_swz))) << 4) + (c & 3) * 4);
+        }
         // the weight slot is free once every lane's loads have been performed (shared-memory accesses
         // of a warp complete in order, ahead of the arrive)
         __syncwarp();
@@ -863,7 +875,7 @@ int smem_of(int MT) { return MT == 2 ? PLayout<2>::kSmemBytes : PLayout<1>::kSme
 
 bool prefill_supported(const GemmArgs &g) {
   const int64_t tiles = ((g.M + 127) / 128) * ((g.N + BN - 1) / BN);
-  return g.N % 32 == 0 && g.K % 8 == 0 && aligned16(g.a) && aligned16(g.b_q) && aligned16(g.scales) &&
+  return g.N % 32 == 0 && g.K % 8 == 0 && aligned16(g.a) && aligned16(g.b_pp ? g.b_pp : g.b_q) && aligned16(g.scales) &&
          aligned16(g.out) && (g.qzeros == nullptr || aligned16(g.qzeros)) && (g.bias == nullptr || aligned16(g.bias)) &&
          tiles <= 0x7fffffff;
 }
@@ -1007,9 +1019,12 @@ bool prefill_weight_maps(const GemmArgs &g, WeightMaps *wm) {
   const int64_t NW = g.N / 8, ng = g.K / g.group_size;
   const bool two = g.group_size < BK && g.group_size != g.K;  // G = 32: two groups per K block
   const int srows = two ? 2 : 1;
-  if (!tma_encode_2d(&wm->tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK, false) ||
-      !tma_encode_2d(&wm->tS, 2, g.scales, g.N, ng, g.N * 2, BN, srows, false))
+  if (!tma_encode_2d(&wm->tS, 2, g.scales, g.N, ng, g.N * 2, BN, srows, false)) return false;
+  if (g.b_pp) {
+    wm->tP = wm->tS;  // unused: prepacked weights travel by plain bulk copies
+  } else if (!tma_encode_2d(&wm->tP, 4, g.b_q, NW, g.K, NW * 4, BN / 8, BK, false)) {
     return false;
+  }
   if (g.qzeros) {
     if (!tma_encode_2d(&wm->tZ, 4, g.qzeros, NW, ng, NW * 4, BN / 8, srows, false)) return false;
   } else {
@@ -1072,6 +1087,8 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl, const
   prm.csplit = pl.k_split > 1 ? pl.k_split : 1;
   prm.a_rows = a_rows;
   prm.dp_waves = pl.stream_k ? prefill_dp_waves(prm.tiles, prm.nk, pl.grid) : 0;
+  prm.b_pp = reinterpret_cast<const uint8_t *>(g.b_pp);
+  prm.pp_tile_bytes = int64_t(prm.nk) * kPBytesHost;
   if (prm.csplit > 1 && (MT != 1 || pl.stream_k || pl.grid % prm.csplit != 0 || prm.nk < prm.csplit))
     return cudaErrorInvalidValue;
 

@@ -23,6 +23,9 @@ struct GemmArgs {
   cudaStream_t stream;
   void *workspace = nullptr;     // optional caller-owned scratch (w4a16_gemm_ws)
   size_t workspace_bytes = 0;
+  // Weights in the prepacked layout (w4a16_prepack) instead of b_q: 64-row x 32-word blocks, tile-
+  // major, each 8 KB contiguous and already in the shared-memory order the kernels read.
+  const int32_t *b_pp = nullptr;
 };
 
 struct DeviceInfo {
@@ -51,6 +54,11 @@ bool tma_available();
 cudaError_t launch_pack(const uint8_t *q, int32_t *packed, int64_t rows, int64_t n, cudaStream_t s);
 cudaError_t launch_unpack(const int32_t *packed, uint8_t *q, int64_t rows, int64_t n, cudaStream_t s);
 cudaError_t launch_repack_k_to_n(const int32_t *k_packed, int32_t *b_q, int64_t k, int64_t n, cudaStream_t s);
+cudaError_t launch_prepack(const int32_t *b_q, int32_t *b_pp, int64_t k, int64_t n, cudaStream_t s);
+// Bytes of the prepacked layout of a [k, n] weight matrix (K and N padded to 64 and 256).
+inline size_t prepack_bytes(int64_t k, int64_t n) {
+  return static_cast<size_t>((n + 255) / 256) * static_cast<size_t>((k + 63) / 64) * 8192u;
+}
 cudaError_t launch_dequant(const int32_t *b_q, const void *scales, const int32_t *qzeros, int64_t k,
                            int64_t n, int group_size, int zp_bias, int dtype, void *w_out,
                            cudaStream_t s);

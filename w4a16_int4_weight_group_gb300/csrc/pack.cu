@@ -1,4 +1,5 @@
-// Layout kernels: pack / unpack of 4-bit values eight per int32 along the last dimension, and the
+// Layout kernels: pack / unpack of 4-bit values eight per int32 along the last dimension, the
+// K-packed -> N-packed repack, this library's prepacked (kernel-native) weight layout, and the
 // materialised dequantisation W[k, n] = RNE_dtype((q - zp) * s).
 //
 // Packing: nibble j (bits 4j..4j+3) of word c holds column 8c+j - the plain reading of "eight values
@@ -64,6 +65,24 @@ __global__ void repack_k_to_n_kernel(const int32_t *__restrict__ kp, int32_t *__
   }
 }
 
+// Prepacked layout: one thread per destination word. Destination word i is position `pos` of row r
+// of the 64 x 32-word block kb of column tile t (blocks tile-major, 2048 words each); it holds word
+// w = 4 * ((pos / 4) ^ (r % 8)) + pos % 4 of the tile's row, i.e. b_q[64 kb + r][32 t + w], or zero
+// past K or N/8.
+__global__ void prepack_kernel(const int32_t *__restrict__ b_q, int32_t *__restrict__ b_pp, int64_t K, int64_t nw,
+                               int64_t kbs, int64_t total) {
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int pos = static_cast<int>(i & 31);
+    const int r = static_cast<int>((i >> 5) & 63);
+    const int64_t blk = i >> 11;  // (t, kb)
+    const int64_t t = blk / kbs, kb = blk - t * kbs;
+    const int w = 4 * ((pos >> 2) ^ (r & 7)) + (pos & 3);
+    const int64_t k = kb * 64 + r, c = t * 32 + w;
+    b_pp[i] = (k < K && c < nw) ? b_q[k * nw + c] : 0;
+  }
+}
+
 template <class DT>
 __global__ void dequant_kernel(const int32_t *__restrict__ b_q, const uint16_t *__restrict__ scales,
                                const int32_t *__restrict__ qzeros, int64_t K, int64_t N, int G,
@@ -111,6 +130,15 @@ cudaError_t launch_repack_k_to_n(const int32_t *k_packed, int32_t *b_q, int64_t 
   const int64_t blocks = (k / 8) * (n / 8);
   if (blocks == 0) return cudaSuccess;
   repack_k_to_n_kernel<<<grid_for(blocks), kThreads, 0, s>>>(k_packed, b_q, k, n);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepack(const int32_t *b_q, int32_t *b_pp, int64_t k, int64_t n, cudaStream_t s) {
+  const int64_t nw = n / 8, kbs = (k + 63) / 64, tiles = (nw + 31) / 32;
+  const int64_t total = tiles * kbs * 2048;
+  if (total == 0) return cudaSuccess;
+  prepack_kernel<<<grid_for(total), kThreads, 0, s>>>(b_q, b_pp, k, nw, kbs, total);
   note_launch();
   return cudaGetLastError();
 }
