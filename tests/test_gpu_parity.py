@@ -408,7 +408,10 @@ DECODE_VARIANTS = [(ncg, C, sb) for ncg in (1, 2) for (C, sb) in ((1, 4), (2, 2)
                                                  (8, 2560, 3840, 128, "f16", True, True),
                                                  (3, 5120, 1024, 5120, "bf16", True, False),
                                                  (16, 1024, 2048, 64, "f16", False, True),
-                                                 (12, 4104, 288, 4104, "f16", True, True)])
+                                                 (12, 4104, 288, 4104, "f16", True, True),
+                                                 (8, 1024, 768, 32, "f16", True, True),
+                                                 (2, 640, 512, 64, "bf16", True, False),
+                                                 (7, 4104, 288, 4104, "bf16", True, False)])
 def test_every_decode_configuration_matches_oracle(w, M, K, N, G, dt, asym, bias):
     """Each decode configuration (one or two consumer groups, split-K factors up to 16 with the
     split-K exchange through st.async pushes, stages of 1, 2 or 4 K blocks) against the oracle on the
