@@ -209,7 +209,10 @@ w4a16_status w4a16_gemm_ws(const void *a, const int32_t *b_q, const void *scales
  *   clears the part that must start at zero (the flags) on `stream` first. Calls that overlap on the
  *   GPU (other streams, other threads, graphs replayed concurrently) race on it: serialise them.
  *   A call whose plan needs more scratch than the array holds (stream-K on a device with more than
- *   160 SMs) is rejected with W4A16_ERR_UNSUPPORTED and the sizes in the message.
+ *   160 SMs) is rejected with W4A16_ERR_UNSUPPORTED and the sizes in the message, rather than run
+ *   with a different plan: a call of this entry point always runs the plan that w4a16_gemm_ws runs
+ *   with a large enough workspace, never a slower one in its place. A caller that wants the plan
+ *   without scratch calls w4a16_gemm, which needs no workspace and allocates nothing either.
  * It calls no cudaMalloc, cudaFree or allocating library routine. Arguments, results and other
  * errors are those of w4a16_gemm.
  */
