@@ -231,3 +231,19 @@ def test_decode_planner_picks_the_measured_best_plan(w, shape):
             assert p["path_name"] == "decode"
             assert (p["warps"], p["k_split"], p["k_blocks_per_stage"]) == (9, *MEASURED_BEST_DECODE_PLAN[shape]), p
             assert p["grid"] == -(-N // 256) * p["k_split"]
+
+
+def test_layer_call_marshalling_module_reaches_the_c_abi(w):
+    """The CPython marshalling module of the prepared-layer call (built beside the library) passes its
+    seven integer arguments to w4a16_layer_gemm: a null layer comes back as INVALID_ARG with the
+    library's message, None stands for a null pointer, and a wrong argument count is a TypeError."""
+    mod = pytest.importorskip("w4a16_int4_weight_group_gb300._w4a16_call")
+    fn = w._layer_gemm_fn()
+    assert fn is mod.layer_gemm
+    assert fn(None, 0, 0, 1, None, 0, None) == 1  # W4A16_ERR_INVALID_ARG
+    assert "layer must not be NULL" in w.last_error()
+    assert fn(0, 0, 0, 1, 0, 0, 0) == 1
+    with pytest.raises(TypeError):
+        fn(None, 0, 0)
+    with pytest.raises(TypeError):
+        fn(None, 0, 0, "one", None, 0, None)

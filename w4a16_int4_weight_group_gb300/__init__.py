@@ -120,6 +120,18 @@ def _ptr(t: Optional[torch.Tensor]):
 _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
+def _layer_gemm_fn():
+    """The prepared-layer call: the CPython marshalling module when it was built (it converts the
+    integer arguments with less host time per call than ctypes), else the ctypes function."""
+    L = lib()
+    try:
+        from . import _w4a16_call
+    except ImportError:
+        return L.w4a16_layer_gemm
+    _w4a16_call.bind(ctypes.cast(L.w4a16_layer_gemm, ctypes.c_void_p).value)
+    return _w4a16_call.layer_gemm
+
+
 def _stream(device: torch.device):
     """The current CUDA stream of `device` as a raw handle (without building a Stream object when
     the runtime offers the raw query)."""
@@ -320,7 +332,8 @@ class W4A16Linear:
                                             self.k, self.n, self.code, ctypes.byref(h)))
         self._handle = h.value
         self._lib = L
-        self._gemm = L.w4a16_layer_gemm
+        self._gemm = _layer_gemm_fn()
+        self._dev_index = self.device.index if self.device.index is not None else torch.cuda.current_device()
 
     def __del__(self):
         h = getattr(self, "_handle", None)
@@ -329,23 +342,25 @@ class W4A16Linear:
             self._handle = None
 
     def __call__(self, a: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
-        if (a.dim() != 2 or a.shape[1] != self.k or a.dtype != self.dtype or a.device != self.device
+        # the checks use the cheapest tensor queries (a decode call takes a few microseconds)
+        dev = self._dev_index
+        if (a.dtype is not self.dtype or a.dim() != 2 or a.shape[1] != self.k or a.get_device() != dev
                 or not a.is_contiguous()):
             raise ValueError(f"a must be a contiguous [M, {self.k}] {self.dtype} tensor on {self.device}")
         m = a.shape[0]
         if out is None:
             out = torch.empty((m, self.n), dtype=self.dtype, device=self.device)
-        elif (out.shape != (m, self.n) or out.dtype != self.dtype or out.device != self.device
-              or not out.is_contiguous()):
+        elif (out.dtype is not self.dtype or out.dim() != 2 or out.shape[0] != m or out.shape[1] != self.n
+              or out.get_device() != dev or not out.is_contiguous()):
             raise ValueError(f"out must be a contiguous [{m}, {self.n}] {self.dtype} tensor on {self.device}")
-        stream = _stream(self.device)
+        stream = _raw_stream(dev) if _raw_stream is not None else torch.cuda.current_stream(self.device).cuda_stream
         need = 0
         if self.use_workspace:
             need = self._need.get(m)
             if need is None:
                 need = self._need[m] = int(self._lib.w4a16_layer_workspace_size(self._handle, m))
         if need:
-            ws = workspace_for(self.device, stream.value or 0, need)
+            ws = workspace_for(self.device, stream, need)
             st = self._gemm(self._handle, a.data_ptr(), out.data_ptr(), m, ws.data_ptr(), ws.numel(), stream)
         else:
             st = self._gemm(self._handle, a.data_ptr(), out.data_ptr(), m, None, 0, stream)

@@ -10,6 +10,7 @@ import os
 import shutil
 import subprocess
 import sys
+import sysconfig
 from concurrent.futures import ThreadPoolExecutor
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -20,6 +21,10 @@ OBJ_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libw4a16.so")
 
 SOURCES = ["api.cu", "pack.cu", "gemm_generic.cu", "gemm_decode.cu", "gemm_prefill.cu"]
+# CPython argument marshalling for the prepared-layer call (optional: the binding uses ctypes when it
+# cannot be built, e.g. without the Python headers)
+PYCALL_SRC = os.path.join(CSRC, "pycall.c")
+PYCALL_PATH = os.path.join(HERE, "_w4a16_call" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
                      "-I", INCLUDE, "-Xptxas", "-warn-spills"]
@@ -33,7 +38,7 @@ def _nvcc() -> str:
 
 
 def _deps():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h"))]
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h", ".c"))]
     files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     files.append(os.path.abspath(__file__))
     return files
@@ -46,8 +51,27 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
+def build_pycall(force: bool = False) -> bool:
+    """Compile the CPython marshalling module beside the library; False when it cannot be built."""
+    if not force and os.path.exists(PYCALL_PATH) and os.path.getmtime(PYCALL_PATH) >= os.path.getmtime(PYCALL_SRC):
+        return True
+    inc = sysconfig.get_paths().get("include")
+    if not inc or not os.path.exists(os.path.join(inc, "Python.h")):
+        return False
+    cc = shutil.which(os.environ.get("CC", "cc")) or shutil.which("gcc")
+    if not cc:
+        return False
+    tmp = PYCALL_PATH + ".tmp"
+    r = subprocess.run([cc, "-O2", "-shared", "-fPIC", "-I", inc, PYCALL_SRC, "-o", tmp], capture_output=True, text=True)
+    if r.returncode != 0:
+        return False
+    os.replace(tmp, PYCALL_PATH)
+    return True
+
+
 def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -> str:
-    """Compile and link libw4a16.so (sm_103a). Returns the library path."""
+    """Compile and link libw4a16.so (sm_103a) and the marshalling module. Returns the library path."""
+    build_pycall(force)
     if not force and up_to_date():
         return LIB_PATH
     nvcc = _nvcc()

@@ -218,6 +218,26 @@ bool tma_available() { return tma_encoder() != nullptr; }
 
 bool tma_encode_2d(CUtensorMap *map, int elem_bytes, const void *ptr, uint64_t inner, uint64_t outer,
                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle_128b) {
+  // The descriptor is a pure function of these arguments, and the calls of a model step encode the
+  // same activation and output views step after step: each thread keeps its last eight encodings.
+  struct Memo {
+    CUtensorMap map;
+    const void *ptr;
+    uint64_t inner, outer, row_bytes;
+    uint32_t box_inner, box_outer;
+    int elem_bytes;
+    bool swizzle, valid;
+  };
+  thread_local Memo memo[8];
+  thread_local unsigned memo_next = 0;
+  for (const Memo &m : memo) {
+    if (m.valid && m.ptr == ptr && m.inner == inner && m.outer == outer && m.row_bytes == row_bytes &&
+        m.box_inner == box_inner && m.box_outer == box_outer && m.elem_bytes == elem_bytes &&
+        m.swizzle == swizzle_128b) {
+      *map = m.map;
+      return true;
+    }
+  }
   const EncodeFn enc = tma_encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {inner, outer};
@@ -225,9 +245,13 @@ bool tma_encode_2d(CUtensorMap *map, int elem_bytes, const void *ptr, uint64_t i
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
-  return enc(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             swizzle_128b ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (enc(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          swizzle_128b ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Memo &m = memo[memo_next++ & 7u];
+  m = Memo{*map, ptr, inner, outer, row_bytes, box_inner, box_outer, elem_bytes, swizzle_128b, true};
+  return true;
 }
 
 cudaError_t current_device_info(DeviceInfo *info) {
