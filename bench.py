@@ -195,7 +195,7 @@ def profile_traffic(kernel_tag, workload):
 
 
 def dominant_kernel(name):
-    return "gemm_prefill" if name in ("prefill", "mid_m", "sweep") else "gemm_decode"
+    return "gemm_prefill" if name in ("prefill", "sweep") else "gemm_decode"
 
 
 def workload_config(name, per_graph=None):

@@ -68,7 +68,7 @@ typedef enum {
 typedef enum {
   W4A16_PATH_NONE = 0,    /* M == 0: nothing to do                                            */
   W4A16_PATH_GENERIC = 1, /* any alignment: one thread per (8 output columns, 8 rows), K-sliced   */
-  W4A16_PATH_DECODE = 2,  /* M <= 16: split-K skinny GEMM, TMA weight stream, ldmatrix.trans +
+  W4A16_PATH_DECODE = 2,  /* M <= 32: split-K skinny GEMM, TMA weight stream, ldmatrix.trans +
                              in-register magic-number dequant, mma.sync, cluster (DSMEM) split-K */
   W4A16_PATH_PREFILL = 3  /* large M: TMA-fed tcgen05/TMEM GEMM, int4 tiles dequantised into
                              shared memory before each UMMA                                     */

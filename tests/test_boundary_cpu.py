@@ -136,9 +136,13 @@ def test_prefill_plan_stream_k_with_a_workspace(w):
     # few tiles: fewer CTAs than SMs, so that the owner's fix-up stays short
     p = w.w4a16_plan(256, 4096, 1024, 32, 1, True, 152)
     assert p["stream_k"] == 1 and 4 < p["grid"] < 152, p
-    # mid M (17..128): one CTA per 128-row tile would leave most SMs idle; clusters of CTAs split each
+    # 17..32 rows: the decode kernel with four row tiles (one CTA per SM)
+    for m in (17, 24, 32):
+        p = w.w4a16_plan(m, 5120, 7168, 128, 1, False, 152)
+        assert p["path_name"] == "decode" and p["m_tile"] == 32 and p["warps"] == 9 and p["grid"] <= 152, (m, p)
+    # mid M (33..128): one CTA per 128-row tile would leave most SMs idle; clusters of CTAs split each
     # tile's K blocks and add their partial tiles through distributed shared memory (no workspace)
-    for m in (17, 32, 64, 128):
+    for m in (33, 64, 128):
         for ws in (True, False):
             p = w.w4a16_plan(m, 5120, 7168, 128, 1, False, 152, with_workspace=ws)
             assert p["path_name"] == "prefill" and p["m_tile"] == 128 and p["stream_k"] == 0, (m, p)
@@ -247,3 +251,23 @@ def test_layer_call_marshalling_module_reaches_the_c_abi(w):
         fn(None, 0, 0)
     with pytest.raises(TypeError):
         fn(None, 0, 0, "one", None, 0, None)
+
+
+# 17..32 rows (four row tiles, one CTA per SM): the splits measured fastest on GB300 for the mid-M
+# layers (per-call time of CUDA-graph chains; cluster sizes 3..10 tried at M = 17, 24 and 32)
+MEASURED_BEST_DECODE_J4_SPLIT = {
+    (5120, 7168, 128): 4,     # 112 CTAs, 13.6-13.9 us (the 128-row kernel: 17.0-17.9 us)
+    (17408, 5120, 128): 6,    # 120 CTAs, 28.7-29.0 us (32.8-33.2 us)
+    (2560, 19456, 128): 2,    # 152 CTAs, 15.5-16.2 us (18.6-19.0 us)
+}
+
+
+@pytest.mark.parametrize("shape", sorted(MEASURED_BEST_DECODE_J4_SPLIT))
+def test_decode_planner_four_row_tiles(w, shape):
+    K, N, G = shape
+    for M in (17, 24, 32):
+        p = w.w4a16_plan(M, K, N, G, 1, False, 152, False)
+        assert p["path_name"] == "decode" and p["m_tile"] == 32 and p["warps"] == 9, p
+        assert p["k_split"] == MEASURED_BEST_DECODE_J4_SPLIT[shape], p
+        # never a cluster size whose clusters pack badly, and one wave of CTAs
+        assert p["k_split"] in (1, 2, 4, 6, 8) and p["grid"] <= 152, p

@@ -62,7 +62,7 @@ def test_compiled_op_uses_runtime_m(ops):
         out = fn(bits_to_torch(c.a, "f16"))
         torch.cuda.synchronize()
         rows = np.unique(np.linspace(0, M - 1, 6).astype(int))
-        want = "decode" if M <= 16 else "prefill"
+        want = "decode" if M <= 32 else "prefill"
         assert w4.w4a16_plan(M, K, N, G, 0, True, 0)["path_name"] == want
         check_against_oracle(c, torch_to_bits(out), rows=rows, cols=np.arange(0, N, 7), label=f"compiled M={M}",
                              path=want)

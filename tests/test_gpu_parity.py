@@ -165,7 +165,7 @@ def test_zp_bias_values(w, zp):
 
 def test_dispatch_threshold_neighbours(w):
     # every switch point of the dispatcher, +-1
-    for M in (1, 8, 9, 16, 17, 64, 65, 128, 129):
+    for M in (1, 8, 9, 16, 17, 32, 33, 64, 65, 128, 129):
         c = synth.make_case(M, 512, 1024, 128, "bf16", asym=True, seed=M)
         check_against_oracle(c, run(w, c), label=f"M={M}", path=path_taken(w, c))
 
@@ -411,7 +411,10 @@ DECODE_VARIANTS = [(ncg, C, sb) for ncg in (1, 2) for (C, sb) in ((1, 4), (2, 2)
                                                  (12, 4104, 288, 4104, "f16", True, True),
                                                  (8, 1024, 768, 32, "f16", True, True),
                                                  (2, 640, 512, 64, "bf16", True, False),
-                                                 (7, 4104, 288, 4104, "bf16", True, False)])
+                                                 (7, 4104, 288, 4104, "bf16", True, False),
+                                                 (17, 1024, 2048, 64, "f16", True, True),
+                                                 (24, 2112, 1152, 32, "bf16", False, False),
+                                                 (32, 4104, 288, 4104, "bf16", True, False)])
 def test_every_decode_configuration_matches_oracle(w, M, K, N, G, dt, asym, bias):
     """Each decode configuration (one or two consumer groups, split-K factors up to 16 with the
     split-K exchange through st.async pushes, stages of 1, 2 or 4 K blocks) against the oracle on the

@@ -1,4 +1,4 @@
-// Decode / skinny path of the W4A16 product (M <= 16): a split-K GEMM that streams the packed
+// Decode / skinny path of the W4A16 product (M <= 32): a split-K GEMM that streams the packed
 // weights once from HBM through TMA, dequantises them in registers and multiplies on the tensor cores.
 //
 // Where the ideas come from: the PR #40977 report (implementation breakdown item 3) describes a
@@ -7,16 +7,18 @@
 // the GPU idle. What this kernel does on sm_103a:
 //
 //  * Work split. A CTA owns 256 output columns and a contiguous range of K blocks (64 rows each);
-//    the C CTAs of one thread-block cluster split K. Seventeen warps: one TMA producer and sixteen
-//    consumers in two groups of eight that take alternate K blocks; consumer w of a group owns
-//    columns [32w, 32w+32) of the tile. The second group hands its sums to the first through
-//    shared memory, and cluster ranks add their partial tiles through distributed shared memory,
-//    both in a fixed order: deterministic, and no global scratch memory.
+//    the C CTAs of one thread-block cluster split K. Nine warps: one TMA producer and eight
+//    consumers; consumer w owns columns [32w, 32w+32) of the tile. (A variant with two groups of
+//    eight consumers on alternate stages is kept for tests and tuning.) Cluster ranks add their
+//    partial tiles through distributed shared memory in a fixed order: deterministic, and no global
+//    scratch memory.
 //  * Streaming. Per K block one TMA box of packed weights (64 rows x 128 bytes, 128-byte swizzle),
-//    the activation rows (8 or 16 x 64, zero-filled past M), and the scale and zero-point rows of the
-//    block's one or two groups land in a 16-deep ring of shared-memory stages guarded by full/empty
-//    mbarriers; the producer runs up to 16 blocks ahead of the consumers, with at most 8 blocks
-//    (64 KB of weights per CTA) requested and not yet landed.
+//    the activation rows (8, 16 or 32 x 64, zero-filled past M), and the scale and zero-point rows of
+//    the block's one or two groups land in an 8-block ring of shared-memory stages guarded by
+//    full/empty mbarriers; at most 8 blocks (64 KB of weights per CTA) are requested and not yet
+//    landed. With up to 16 rows a CTA takes under half of an SM, so a CTA of the next call (launched
+//    early under programmatic dependent launch) is resident beside it and requests its first weights
+//    before the dependency wait; with 17..32 rows a CTA takes a whole SM.
 //  * Fragments. Viewing a packed row as 16-bit elements (4 nibbles = 4 consecutive columns each),
 //    ldmatrix.trans delivers to lane (g, t) the element of rows 2t and 2t+1 for column quad g: the
 //    two rows of a k pair side by side, which is what a 16-bit MMA register holds. The 128-byte
@@ -26,12 +28,15 @@
 //    high nibble of a byte) or a bf16 pair with exponent of 128: exactly (base+q_k, base+q_k+1). One
 //    packed subtraction of (base + zp) leaves q - zp, a small integer and so exact in 16 bits. The
 //    tensor core multiplies these by the activations (blk = sum_k A (q - zp) in fp32); per K block
-//    and group, in fp32: acc += s * blk. The scale is applied in fp32, so the weights are never
+//    and group, in fp32: acc += s * blk. With up to 8 rows and one scale group per K block the
+//    subtraction moves out of the loop: the MMAs take the magic values (base + q) as they are, one
+//    more MMA against a ones operand gives the row sums rs = sum_k A, and at the end of a group
+//    acc += s * (blk - (base + zp) * rs). The scale is applied in fp32, so the weights are never
 //    rounded to 16 bits; with one-hot activations the result is exactly RNE(s * (q - zp)), the value
 //    w4a16_dequant writes.
 //  * Multiply. mma.sync m16n8k16 with 16 output columns as the MMA rows and up to 8 rows of A as the
-//    MMA columns (the M <= 8 decode batch fills the n=8 side; M <= 16 takes two MMAs). Per warp and
-//    K block: 8 LOP3-based unpacks of 8 weights each, 32 packed subtractions, 8 MMAs and 8 FFMAs.
+//    MMA columns (the M <= 8 decode batch fills the n=8 side; 9..16 rows take two MMAs per step,
+//    17..32 rows four).
 //  * Epilogue. Bias is added in fp32 and the sum rounded once to the activation dtype (PR #40977
 //    report, key source snippets, test reference).
 //  * Every mbarrier wait is bounded: on expiry the CTA records an error word, its warps leave the
@@ -157,7 +162,7 @@ __host__ __device__ constexpr float magic_base(int j) {
 }
 
 template <class DT, int J, bool HAS_ZP, bool TWO_GROUPS, int SBS, int NCG>
-__global__ void __launch_bounds__(threads_of(NCG), NCG == 1 ? 2 : W4A16_DEC_MINB2)
+__global__ void __launch_bounds__(threads_of(NCG), NCG == 1 ? (J >= 4 ? 1 : 2) : W4A16_DEC_MINB2)
     decode_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmP,
                   const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ,
                   const DecodeParams p) {
@@ -203,16 +208,18 @@ __global__ void __launch_bounds__(threads_of(NCG), NCG == 1 ? 2 : W4A16_DEC_MINB
   // live groups among [0, x): lanes with tig < ceil((rows - 8 jt) / 2), in 32-lane runs per jt
   auto live_below = [&](int x) {
     const int rr = static_cast<int>(rows);
-    const int l0 = min(4, (rr + 1) / 2);
-    const int l1 = J == 2 ? max(0, min(4, (rr - 8 + 1) / 2)) : 0;
-    const int span = 32 * J;
-    const int per_span = 8 * l0 + (J == 2 ? 8 * l1 : 0);
-    const int r = x % span;
-    int c = (x / span) * per_span;
-    if (r < 32) {
-      c += (r / 4) * l0 + min(r % 4, l0);
-    } else {
-      c += 8 * l0 + ((r - 32) / 4) * l1 + min((r - 32) % 4, l1);
+    int lj[J], per_span = 0;
+#pragma unroll
+    for (int jt = 0; jt < J; ++jt) {
+      lj[jt] = max(0, min(4, (rr - 8 * jt + 1) / 2));
+      per_span += 8 * lj[jt];
+    }
+    int c = (x / (32 * J)) * per_span, r = x % (32 * J);
+#pragma unroll
+    for (int jt = 0; jt < J; ++jt) {
+      const int rj = min(r, 32);
+      c += (rj / 4) * lj[jt] + min(rj % 4, lj[jt]);
+      r -= rj;
     }
     return c;
   };
@@ -651,6 +658,10 @@ KernelFn pick_zg(bool zp, bool two) {
 }
 template <class DT, int SBS, int NCG>
 KernelFn pick_j(int J, bool zp, bool two) {
+  if (J == 4) {  // 17..32 rows: one consumer group only
+    if constexpr (NCG == 1) return pick_zg<DT, 4, SBS, 1>(zp, two);
+    return nullptr;
+  }
   return J == 1 ? pick_zg<DT, 1, SBS, NCG>(zp, two) : pick_zg<DT, 2, SBS, NCG>(zp, two);
 }
 template <class DT, int NCG>
@@ -666,14 +677,14 @@ KernelFn pick(int dtype, int J, bool zp, bool two, int sb, int ncg) {
   return dtype == W4A16_BF16 ? pick_dt<BF16>(J, zp, two, sb, ncg) : pick_dt<F16>(J, zp, two, sb, ncg);
 }
 int smem_of(int J, int ncg) {
-  if (ncg == 1) return J == 1 ? Layout<1, 1>::kSmem : Layout<2, 1>::kSmem;
+  if (ncg == 1) return J == 1 ? Layout<1, 1>::kSmem : (J == 2 ? Layout<2, 1>::kSmem : Layout<4, 1>::kSmem);
   return J == 1 ? Layout<1, 2>::kSmem : Layout<2, 2>::kSmem;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool decode_supported_impl(const GemmArgs &g) {
-  return g.M <= 16 && g.N % 32 == 0 && g.K % 8 == 0 && aligned16(g.a) && aligned16(g.b_pp ? g.b_pp : g.b_q) &&
+  return g.M <= 32 && g.N % 32 == 0 && g.K % 8 == 0 && aligned16(g.a) && aligned16(g.b_pp ? g.b_pp : g.b_q) &&
          aligned16(g.scales) && (g.qzeros == nullptr || aligned16(g.qzeros));
 }
 
@@ -705,7 +716,7 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
                       w4a16_plan_t *p) {
   (void)group_size;
   (void)query_device;
-  const int J = M <= 8 ? 1 : 2;
+  const int J = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
   const int64_t n_tiles = (N + BN - 1) / BN;
   const int64_t kbt = (K + BK - 1) / BK;
   const double sms = double(num_sms > 0 ? num_sms : 1);
@@ -719,7 +730,17 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
   // leave the next call no room to start early - and f = 0.88 for two-block stages on ranks of at
   // least 8 blocks, 0.97 on ranks of 4 to 7 (a stage wait per two blocks), 1 for one-block stages.
   // Every rank keeps at least two K blocks.
+  //   With 17..32 rows (four row tiles) a CTA needs more registers and shared memory than half an SM:
+  // one CTA per SM, about 0.6 us per K block, stages of one or two blocks alike, and cluster sizes
+  // from {1, 2, 4, 6, 8} only (measured: clusters of 5 and 7 CTAs of this size ran 1.3-1.7x slower
+  // than their share of blocks predicts). A wave holds as many CTAs as clusters of that size fit at
+  // once on GB300 (measured with cudaOccupancyMaxActiveClusters for one CTA per SM: 152, 152, 144,
+  // 138 and 120 of the 152 SMs for C = 1, 2, 4, 6, 8), scaled by the SM count.
   int ncg = 1;
+  auto j4_capacity = [&](int C) -> double {
+    const double frac = C <= 2 ? 1.0 : (C == 4 ? 144.0 / 152 : (C == 6 ? 138.0 / 152 : (C == 8 ? 120.0 / 152 : 0.0)));
+    return std::floor(sms * frac / C) * C;
+  };
   int bestC = 1, bestSB = 1;
   double best = -1.0;
   for (int Ct = 1; Ct <= kMaxCluster; ++Ct) {
@@ -732,10 +753,17 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
       if (C > 1 && kb < 2) continue;
       if (sb == 2 && kb < 4) continue;
       const double grid = double(n_tiles * C);
-      const double waves = std::ceil(grid / (2.0 * sms));
-      const double over = std::max(0.0, grid - sms) / sms;
-      const double f = sb == 2 ? (kb >= 8 ? 0.88 : 0.97) : 1.0;
-      const double cost = (0.16 * C + 0.47 * double(kb) * waves + 0.45 * double(kb) * over) * f;
+      double cost;
+      if (J == 4) {
+        const double cap = j4_capacity(C);
+        if (cap <= 0.0) continue;
+        cost = 0.16 * C + 0.6 * double(kb) * std::ceil(grid / cap);
+      } else {
+        const double waves = std::ceil(grid / (2.0 * sms));
+        const double over = std::max(0.0, grid - sms) / sms;
+        const double f = sb == 2 ? (kb >= 8 ? 0.88 : 0.97) : 1.0;
+        cost = (0.16 * C + 0.47 * double(kb) * waves + 0.45 * double(kb) * over) * f;
+      }
       if (best < 0 || cost < best - 1e-9) {
         best = cost;
         bestC = C;
@@ -743,7 +771,7 @@ void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_s
       }
     }
   }
-  if (const int o = g_ovr_ncg.load(std::memory_order_relaxed)) ncg = o;
+  if (const int o = g_ovr_ncg.load(std::memory_order_relaxed)) ncg = J == 4 ? 1 : o;
   if (const int oc = g_ovr_c.load(std::memory_order_relaxed)) {
     int64_t kb = kbt;
     rank_shape(kbt, oc, &bestSB, &kb, g_ovr_sb.load(std::memory_order_relaxed));
@@ -804,10 +832,11 @@ cudaError_t launch_gemm_decode(const GemmArgs &g, const w4a16_plan_t &pl, const 
     wm = &own;
   }
   const KernelFn fn = pick(g.dtype, J, zp, two, sb, ncg);
+  if (!fn) return cudaErrorInvalidValue;  // 17..32 rows run with one consumer group only
   const int smem = smem_of(J, ncg);
   {
     static std::mutex mu;
-    static bool configured[64][2][2][2][2][3][2] = {};
+    static bool configured[64][2][4][2][2][3][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
