@@ -380,17 +380,22 @@ def test_plans_of_different_shapes_share_one_workspace(w):
                                            (128, 17408, 5120, 17408, "bf16", True), (17, 1152, 2112, 32, "bf16", False)])
 def test_cluster_split_k_mid_m(w, M, K, N, G, dt, asym):
     """Mid M: the CTAs of a cluster split each 128-row tile's K blocks and add their partial tiles
-    through distributed shared memory in rank order: oracle parity, determinism, no workspace."""
+    through distributed shared memory in rank order: oracle parity, determinism, no workspace. (At
+    17..32 rows the dispatcher runs the decode kernel; the 128-row kernel is forced there.)"""
     c = synth.make_case(M, K, N, G, dt, asym=asym, bias=True, seed=M + 3)
     code = 1 if dt == "bf16" else 0
-    plan = w.w4a16_plan(M, K, N, G, code, asym, 0, with_workspace=False)
-    assert plan["path_name"] == "prefill" and plan["k_split"] > 1 and plan["stream_k"] == 0, plan
-    t = case_tensors(c)
-    outs = []
-    for _ in range(2):
-        out = w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"], use_workspace=False)
-        torch.cuda.synchronize()
-        outs.append(torch_to_bits(out))
+    w.w4a16_debug_force_path("prefill" if M <= 32 else None)
+    try:
+        plan = w.w4a16_plan(M, K, N, G, code, asym, 0, with_workspace=False)
+        assert plan["path_name"] == "prefill" and plan["k_split"] > 1 and plan["stream_k"] == 0, plan
+        t = case_tensors(c)
+        outs = []
+        for _ in range(2):
+            out = w.w4a16_gemm(t["a"], t["b_q"], t["scales"], t["qzeros"], G, 8, t["bias"], use_workspace=False)
+            torch.cuda.synchronize()
+            outs.append(torch_to_bits(out))
+    finally:
+        w.w4a16_debug_force_path(None)
     assert np.array_equal(outs[0], outs[1]), "cluster split-K must be deterministic"
     assert w.w4a16_get_device_error() == 0
     rng = np.random.default_rng(M)
