@@ -302,7 +302,8 @@ w4a16_status w4a16_debug_force_path(int path);
 /*
  * w4a16_debug_decode_override - fixes parts of the decode path's launch plan for tests and tuning:
  * consumer_groups (1: one group of eight consumer warps per CTA and an 8-block ring, so that two CTAs
- * fit on an SM; 2: two groups and a 16-block ring), k_split (the CTAs of a cluster that split K,
+ * fit on an SM up to 16 rows; 2: two groups and a 16-block ring, up to 16 rows; calls of 17..32 rows
+ * always run one group), k_split (the CTAs of a cluster that split K,
  * 1..16; the rank ranges are rounded to whole stages, which may leave fewer ranks) and
  * k_blocks_per_stage (1, 2 or 4). 0 leaves a field to the dispatcher; all zero restores the
  * automatic plan. Process-wide. Errors: INVALID_ARG for values outside those ranges.

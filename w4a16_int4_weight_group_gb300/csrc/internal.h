@@ -73,7 +73,7 @@ struct WeightMaps {
   int key;
 };
 
-// Decode path (M <= 16): plan fields m_tile and k_split are honoured.
+// Decode path (M <= 32): plan fields m_tile and k_split are honoured.
 bool decode_supported(const GemmArgs &g);
 // query_device: use the runtime's occupancy queries (needs a device); otherwise assume 2 CTAs per SM.
 void decode_make_plan(int64_t M, int64_t K, int64_t N, int group_size, int num_sms, bool query_device,
