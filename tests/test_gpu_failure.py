@@ -28,7 +28,7 @@ def w():
 
 
 @pytest.mark.parametrize("path,M,K,N", [("prefill", 256, 4096, 1024), ("prefill", 64, 4096, 1024), ("decode", 4, 4096, 1024),
-                                        ("decode", 1, 2560, 19456)])
+                                        ("decode", 1, 2560, 19456), ("decode", 24, 4096, 1024)])
 def test_bounded_wait_reports_timeout_and_recovers(w, path, M, K, N):
     c = synth.make_case(M, K, N, 128, "bf16", asym=True, seed=21)
     t = case_tensors(c)
