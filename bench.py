@@ -319,30 +319,30 @@ class Workload:
             if pp:  # the prepacked layers keep their own copies; the canonical replicas are not needed
                 b_qs = None
             self.pools[key] = {"layers": layers, "reps": reps, "keep": (b_qs, scs, qzs, bi)}
-        # activations and outputs of all the calls of a step: one device buffer per dtype (16-byte
-        # aligned slices), mirrored by pinned host buffers; the end-to-end leg moves a step's inputs
-        # with one host-to-device copy per dtype and its results with one device-to-host copy per dtype
-        a_elems, o_elems = {}, {}
-        for (M, K, N, G, dt, *_r) in cases:
-            a_elems[dt] = a_elems.get(dt, 0) + ((M * K + 7) // 8) * 8
-            o_elems[dt] = o_elems.get(dt, 0) + ((M * N + 7) // 8) * 8
-        self.a_dev = {dt: torch.empty(n, dtype=tdt[dt], device=dev) for dt, n in a_elems.items()}
-        self.o_dev = {dt: torch.empty(n, dtype=tdt[dt], device=dev) for dt, n in o_elems.items()}
-        self.a_pin = {dt: torch.empty(n, dtype=tdt[dt]).pin_memory() for dt, n in a_elems.items()}
-        self.o_pin = {dt: torch.empty(n, dtype=tdt[dt]).pin_memory() for dt, n in o_elems.items()}
+        # activations and outputs of all the calls of a step: one device byte buffer each (16-byte
+        # aligned slices, viewed in each call's dtype), mirrored by pinned host buffers; the end-to-end
+        # leg moves a step's inputs with one host-to-device copy and its results with one
+        # device-to-host copy
+        def padded(elems):
+            return ((2 * elems + 15) // 16) * 16
+        a_bytes = sum(padded(M * K) for (M, K, *_r) in cases)
+        o_bytes = sum(padded(M * N) for (M, K, N, *_r) in cases)
+        self.a_dev = torch.empty(a_bytes, dtype=torch.uint8, device=dev)
+        self.o_dev = torch.empty(o_bytes, dtype=torch.uint8, device=dev)
+        self.a_pin = torch.empty(a_bytes, dtype=torch.uint8).pin_memory()
+        self.o_pin = torch.empty(o_bytes, dtype=torch.uint8).pin_memory()
         self.calls = []
-        ao = {dt: 0 for dt in a_elems}
-        oo = {dt: 0 for dt in o_elems}
+        ao = oo = 0
         for (M, K, N, G, dt, asym, bias, lo, hi, seed) in cases:
             key = (K, N, G, dt, asym, bias)
             a_host = to_t(synth.activations(M, K, dt, seed=1000 + seed), dt)
-            self.a_pin[dt][ao[dt]:ao[dt] + M * K].copy_(a_host.reshape(-1))
-            a = self.a_dev[dt][ao[dt]:ao[dt] + M * K].view(M, K)
+            self.a_pin[ao:ao + 2 * M * K].view(tdt[dt]).copy_(a_host.reshape(-1))
+            a = self.a_dev[ao:ao + 2 * M * K].view(tdt[dt]).view(M, K)
             a.copy_(a_host)
-            out = self.o_dev[dt][oo[dt]:oo[dt] + M * N].view(M, N)
+            out = self.o_dev[oo:oo + 2 * M * N].view(tdt[dt]).view(M, N)
             self.calls.append({"key": key, "a": a, "out": out, "case": (M, K, N, G, dt, asym, bias)})
-            ao[dt] += ((M * K + 7) // 8) * 8
-            oo[dt] += ((M * N + 7) // 8) * 8
+            ao += padded(M * K)
+            oo += padded(M * N)
         self.counters = {key: 0 for key in self.pools}
 
     def call(self, c):
@@ -353,18 +353,14 @@ class Workload:
 
     def step(self, use_host=False):
         if use_host:
-            for dt, t in self.a_dev.items():
-                t.copy_(self.a_pin[dt], non_blocking=True)
+            self.a_dev.copy_(self.a_pin, non_blocking=True)
         for c in self.calls:
             self.call(c)
         if use_host:
-            for dt, t in self.o_dev.items():
-                self.o_pin[dt].copy_(t, non_blocking=True)
+            self.o_pin.copy_(self.o_dev, non_blocking=True)
 
     def io_bytes(self):
-        h2d = sum(t.numel() * t.element_size() for t in self.a_dev.values())
-        d2h = sum(t.numel() * t.element_size() for t in self.o_dev.values())
-        return h2d, d2h
+        return self.a_dev.numel(), self.o_dev.numel()
 
 
 def _graph_time(fn_per_step, steps, per_graph, stream, dev, barrier=None, world=1):
