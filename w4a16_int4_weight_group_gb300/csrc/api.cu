@@ -95,8 +95,9 @@ int forced_path() {
   return g_forced_path.load(std::memory_order_relaxed);
 }
 
-// M at and above which the tcgen05 path is preferred when it applies.
-constexpr int64_t kPrefillMinM = 65;
+// M at and above which the tcgen05 path is preferred when it applies (the decode kernel takes up to
+// 32 rows: four row tiles of 8).
+constexpr int64_t kPrefillMinM = 33;
 
 // `tma` tells whether the driver's tensor-map encoder is available (the TMA-fed paths need it).
 void choose_plan(const GemmArgs &g, int num_sms, bool tma, bool query_device, bool workspace, w4a16_plan_t *p) {
