@@ -163,6 +163,7 @@ struct PrefillParams {
   uint16_t *out;
   int64_t M, K, N;
   int G;
+  int g_shift;       // log2(G) when G is a power of two; otherwise G == K and every row is in group 0 (31)
   int zp_bias;
   int nk;            // K blocks of 64
   int m_tiles;       // row tiles; tile t covers rows (t % m_tiles) and columns (t / m_tiles)
@@ -262,17 +263,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_con = static_cast<int>(c_fix - blockIdx.x);  // contributors to add
   // Tile and K block of this CTA's units, walked in order by every role (no division per unit: the
   // single MMA-issuing and producer threads are on the critical path): start at unit 0, then step.
+  // The cursor also carries the tile's row and column tile indices (t % m_tiles, t / m_tiles), kept
+  // up to date by additions: the producer needs both every unit.
   struct Cursor {
     int64_t t;
     int kb;
+    int mt;      // row tile
+    int64_t nt;  // column tile
   };
-  const Cursor cur0 = dp_units > 0 ? Cursor{int64_t(blockIdx.x), 0} : Cursor{dp_tiles + s_first, kb_first};
+  const int m_tiles = p.m_tiles;
+  auto cursor_at = [&](int64_t t, int kb) { return Cursor{t, kb, static_cast<int>(t % m_tiles), t / m_tiles}; };
+  const int g_mr = static_cast<int>(G % m_tiles);  // a data-parallel step of G tiles, in row and column tiles
+  const int64_t g_mq = G / m_tiles;
+  const Cursor cur0 = dp_units > 0 ? cursor_at(int64_t(blockIdx.x), 0) : cursor_at(dp_tiles + s_first, kb_first);
+  const Cursor cur_shared = cursor_at(dp_tiles + s_first, kb_first);
   auto step = [&](Cursor &c, int i_next) {  // from unit i_next - 1 to unit i_next
     if (i_next == dp_units) {
-      c = Cursor{dp_tiles + s_first, kb_first};  // the data-parallel tiles are done: the shared ones
+      c = cur_shared;  // the data-parallel tiles are done: the shared ones
     } else if (++c.kb == nk) {
       c.kb = 0;
-      c.t += i_next < dp_units ? G : 1;
+      if (i_next < dp_units) {
+        c.t += G;
+        c.mt += g_mr;
+        c.nt += g_mq;
+      } else {
+        c.t += 1;
+        c.mt += 1;
+      }
+      if (c.mt >= m_tiles) {
+        c.mt -= m_tiles;
+        c.nt += 1;
+      }
     }
   };
 
@@ -366,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_phase(empty_a(s), ((j / SA) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error)) return false;
         if (j > 0) step(ca, j);
         mbar_arrive_expect_tx(full_a(s), tx_a);
-        tma_load_2d(base + kOffA + s * kABytes, &tmA, ca.kb * BK, static_cast<int>((ca.t % p.m_tiles) * BM), full_a(s));
+        tma_load_2d(base + kOffA + s * kABytes, &tmA, ca.kb * BK, ca.mt * BM, full_a(s));
         issued_a = j + 1;
         return true;
       };
@@ -374,23 +395,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_units && run; ++j) {
         const int s = j % SP;
         if (j > 0) step(cp, j);
-        const int64_t tp = cp.t;
         const int kbp = cp.kb;
         run = wait_phase(empty_p(s), ((j / SP) & 1) ^ 1u, abort_flag, limit_ns, &g_prefill_error);
         if (!run) break;
         if constexpr (kShared) {
           // one stage, one barrier: A and the weights of unit j together
           mbar_arrive_expect_tx(full_a(s), tx_a + tx_p);
-          tma_load_2d(base + kOffA + s * kABytes, &tmA, kbp * BK, static_cast<int>((tp % p.m_tiles) * BM), full_a(s));
+          tma_load_2d(base + kOffA + s * kABytes, &tmA, kbp * BK, cp.mt * BM, full_a(s));
           issued_a = j + 1;
         } else {
           mbar_arrive_expect_tx(full_p(s), tx_p);
         }
-        const int n0 = static_cast<int>((tp / p.m_tiles) * BN);
+        const int n0 = static_cast<int>(cp.nt * BN);
         const int k0 = kbp * BK;
-        const int grow = k0 / p.G;
+        const int grow = k0 >> p.g_shift;
         if (p.b_pp)  // prepacked: the block is 8 KB of contiguous words (rows with permuted chunks)
-          bulk_load(base + kOffP + s * kPBytes, p.b_pp + (tp / p.m_tiles) * p.pp_tile_bytes + int64_t(kbp) * kPBytes,
+          bulk_load(base + kOffP + s * kPBytes, p.b_pp + cp.nt * p.pp_tile_bytes + int64_t(kbp) * kPBytes,
                     kPBytes, full_p(s));
         else
           tma_load_2d(base + kOffP + s * kPBytes, &tmP, n0 / 8, k0, full_p(s));
@@ -1082,6 +1102,9 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl, const
   prm.K = g.K;
   prm.N = g.N;
   prm.G = g.group_size;
+  prm.g_shift = 31;
+  for (int sh = 0; sh < 31; ++sh)
+    if ((1 << sh) == g.group_size) prm.g_shift = sh;
   prm.zp_bias = g.zp_bias;
   prm.nk = static_cast<int>((g.K + BK - 1) / BK);
   prm.csplit = pl.k_split > 1 ? pl.k_split : 1;
