@@ -319,6 +319,25 @@ def test_prepared_layer_equals_the_function(w, M, K, N, G, dt, asym):
             assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"m={m}"
     with pytest.raises(ValueError):
         layer(t["a"][:, :8].contiguous())  # wrong K
+    # every argument check of the call, each rejected before anything is launched
+    other = torch.float16 if t["a"].dtype == torch.bfloat16 else torch.bfloat16
+    bad_inputs = [t["a"].reshape(-1),                                   # 1-D
+                  t["a"].to(other)]                                     # dtype
+    if M > 1:
+        bad_inputs.append(t["a"].t().contiguous().t())                  # rows not contiguous
+    for x in bad_inputs:
+        with pytest.raises(ValueError):
+            layer(x)
+    good_out = torch.empty((M, N), dtype=t["a"].dtype, device="cuda")
+    bad_outs = [torch.empty((M, N + 8), dtype=t["a"].dtype, device="cuda"),  # shape
+                torch.empty((M, N), dtype=other, device="cuda")]               # dtype
+    if M > 1:
+        bad_outs.append(torch.empty((N, M), dtype=t["a"].dtype, device="cuda").t())  # not contiguous
+    for o in bad_outs:
+        with pytest.raises(ValueError):
+            layer(t["a"], out=o)
+    got = layer(t["a"], out=good_out)
+    assert got is good_out
 
 
 def test_layer_handle_through_the_c_abi(w):

@@ -342,17 +342,21 @@ class W4A16Linear:
             self._handle = None
 
     def __call__(self, a: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
-        # the checks use the cheapest tensor queries (a decode call takes a few microseconds)
+        # the checks use the cheapest tensor queries, each shape read once (every `.shape` builds a new
+        # size object; a decode call takes a few microseconds)
         dev = self._dev_index
-        if (a.dtype is not self.dtype or a.dim() != 2 or a.shape[1] != self.k or a.get_device() != dev
+        sa = a.shape
+        if (a.dtype is not self.dtype or len(sa) != 2 or sa[1] != self.k or a.get_device() != dev
                 or not a.is_contiguous()):
             raise ValueError(f"a must be a contiguous [M, {self.k}] {self.dtype} tensor on {self.device}")
-        m = a.shape[0]
+        m = sa[0]
         if out is None:
             out = torch.empty((m, self.n), dtype=self.dtype, device=self.device)
-        elif (out.dtype is not self.dtype or out.dim() != 2 or out.shape[0] != m or out.shape[1] != self.n
-              or out.get_device() != dev or not out.is_contiguous()):
-            raise ValueError(f"out must be a contiguous [{m}, {self.n}] {self.dtype} tensor on {self.device}")
+        else:
+            so = out.shape
+            if (out.dtype is not self.dtype or len(so) != 2 or so[0] != m or so[1] != self.n
+                    or out.get_device() != dev or not out.is_contiguous()):
+                raise ValueError(f"out must be a contiguous [{m}, {self.n}] {self.dtype} tensor on {self.device}")
         stream = _raw_stream(dev) if _raw_stream is not None else torch.cuda.current_stream(self.device).cuda_stream
         need = 0
         if self.use_workspace:
