@@ -195,6 +195,20 @@ def test_decode_4b_workload_sampled_columns(w, args):
     check_against_oracle(c, out, cols=cols, label="sampled", path=path_taken(w, c))
 
 
+@pytest.mark.parametrize("args", list(synth.config_cases("mid_m")), ids=_config_ids("mid_m"))
+def test_mid_m_workload_sampled_columns(w, args):
+    """The mid-M workload at full size, on the path the dispatcher picks (the decode kernel with four
+    row tiles for 17..32 rows, the 128-row kernel with cluster split-K above), every row checked on
+    sampled columns."""
+    M, K, N, G, dt, asym, bias, lo, hi, seed = args
+    c = synth.make_case(M, K, N, G, dt, asym=asym, bias=bias, seed=seed, scale_lo=lo, scale_hi=hi)
+    want = "decode" if M <= 32 else "prefill"
+    assert w.w4a16_plan(M, K, N, G, 1 if dt == "bf16" else 0, asym, 0)["path_name"] == want
+    out = run(w, c)
+    cols = sample_cols(N, np.random.default_rng(seed))
+    check_against_oracle(c, out, cols=cols, label="mid_m sampled", path=path_taken(w, c))
+
+
 @pytest.mark.parametrize("args", list(synth.config_cases("prefill")), ids=_config_ids("prefill"))
 def test_prefill_workload_sampled(w, args):
     """The prefill workload at full size, in the launch configuration the benchmark times."""
