@@ -87,6 +87,8 @@ SMALL_CASES = [
     (3, 4096, 96, 4096, "bf16", False, False),    # per-channel, narrow N
     (7, 100, 520, 100, "f16", True, True),        # K and N off every fast-path alignment
     (130, 256, 640, 128, "bf16", True, True),     # prefill-sized M, several tiles
+    (2, 8, 8, 8, "f16", True, True),              # the smallest legal shape: K = G = 8, N = 8
+    (1, 64, 8, 32, "bf16", False, False),         # one packed word of columns
 ]
 
 
