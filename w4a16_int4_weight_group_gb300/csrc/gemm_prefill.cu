@@ -166,8 +166,10 @@ struct PrefillParams {
   int g_shift;       // log2(G) when G is a power of two; otherwise G == K and every row is in group 0 (31)
   int zp_bias;
   int nk;            // K blocks of 64
-  int m_tiles;       // row tiles; tile t covers rows (t % m_tiles) and columns (t / m_tiles)
-  int64_t tiles;     // m_tiles x column tiles
+  int m_tiles;       // row tiles
+  int n_tiles;       // column tiles
+  int64_t tiles;     // m_tiles x n_tiles; tile t covers row tile t % m_tiles and column tile
+                     // t / m_tiles, or (column tiles fastest) column tile t % n_tiles and row tile t / n_tiles
   float *partials;   // stream-K: one fp32 [BM][BN] partial tile per CTA (null when every CTA owns whole tiles)
   unsigned int *flags;  // stream-K: per-CTA "partial ready" flags; zero before and after every launch
   int csplit;        // > 1: clusters of csplit CTAs split each tile's K blocks (128-row tiles only)
@@ -206,7 +208,8 @@ __device__ __forceinline__ void magic4(uint32_t w, uint32_t (&h)[4]) {
   }
 }
 
-template <class DT, bool HAS_ZP, bool TWO_GROUPS, int MT>
+// COLS: consecutive tiles step along the column tiles instead of the row tiles (see the work split).
+template <class DT, bool HAS_ZP, bool TWO_GROUPS, int MT, bool COLS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmP,
                    const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ,
@@ -231,7 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Work units are (tile, K block) pairs. Stream-K plans first run dp_waves whole waves of tiles
   // data-parallel: CTA c takes tiles c, c + G, c + 2G, ..., so the CTAs of a wave step through K
-  // together over neighbouring tiles (row tiles fastest) and share the A and weight slices in L2.
+  // together over neighbouring tiles and share the A and weight slices in L2. A wave sweeps the whole
+  // faster tile dimension, so the host makes that the dimension of the smaller operand (row tiles
+  // when A is the smaller, column tiles - COLS - when the weights are): the operand swept by every
+  // wave then stays in L2 and the larger one is read from HBM about once.
   // The remaining tiles' units, tile-major, are then split into contiguous, even shares (with one CTA
   // per tile every share is a whole tile): a share may start or end inside a tile; the CTA holding a
   // tile's K block 0 owns it and adds the partial tiles of the CTAs that hold the rest (they publish
@@ -263,18 +269,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_con = static_cast<int>(c_fix - blockIdx.x);  // contributors to add
   // Tile and K block of this CTA's units, walked in order by every role (no division per unit: the
   // single MMA-issuing and producer threads are on the critical path): start at unit 0, then step.
-  // The cursor also carries the tile's row and column tile indices (t % m_tiles, t / m_tiles), kept
-  // up to date by additions: the producer needs both every unit.
+  // The cursor also carries the tile's row and column tile indices, kept up to date by additions: the
+  // producer needs both every unit. The faster of the two wraps at F tiles into the slower one.
   struct Cursor {
     int64_t t;
     int kb;
     int mt;      // row tile
     int64_t nt;  // column tile
   };
-  const int m_tiles = p.m_tiles;
-  auto cursor_at = [&](int64_t t, int kb) { return Cursor{t, kb, static_cast<int>(t % m_tiles), t / m_tiles}; };
-  const int g_mr = static_cast<int>(G % m_tiles);  // a data-parallel step of G tiles, in row and column tiles
-  const int64_t g_mq = G / m_tiles;
+  const int F = COLS ? p.n_tiles : p.m_tiles;
+  auto cursor_at = [&](int64_t t, int kb) {
+    if constexpr (COLS) return Cursor{t, kb, static_cast<int>(t / F), t % F};
+    else return Cursor{t, kb, static_cast<int>(t % F), t / F};
+  };
+  const int g_fr = static_cast<int>(G % F);  // a data-parallel step of G tiles: within and across F
+  const int64_t g_fq = G / F;
   const Cursor cur0 = dp_units > 0 ? cursor_at(int64_t(blockIdx.x), 0) : cursor_at(dp_tiles + s_first, kb_first);
   const Cursor cur_shared = cursor_at(dp_tiles + s_first, kb_first);
   auto step = [&](Cursor &c, int i_next) {  // from unit i_next - 1 to unit i_next
@@ -282,17 +291,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       c = cur_shared;  // the data-parallel tiles are done: the shared ones
     } else if (++c.kb == nk) {
       c.kb = 0;
-      if (i_next < dp_units) {
-        c.t += G;
-        c.mt += g_mr;
-        c.nt += g_mq;
+      if constexpr (COLS) {
+        if (i_next < dp_units) {
+          c.t += G;
+          c.nt += g_fr;
+          c.mt += static_cast<int>(g_fq);
+        } else {
+          c.t += 1;
+          c.nt += 1;
+        }
+        if (c.nt >= F) {
+          c.nt -= F;
+          c.mt += 1;
+        }
       } else {
-        c.t += 1;
-        c.mt += 1;
-      }
-      if (c.mt >= m_tiles) {
-        c.mt -= m_tiles;
-        c.nt += 1;
+        if (i_next < dp_units) {
+          c.t += G;
+          c.mt += g_fr;
+          c.nt += g_fq;
+        } else {
+          c.t += 1;
+          c.mt += 1;
+        }
+        if (c.mt >= F) {
+          c.mt -= F;
+          c.nt += 1;
+        }
       }
     }
   };
@@ -625,8 +649,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const bool owner = seg_kb0 == 0;        // holds K block 0: adds the others' partials, stores
         const bool whole = owner && kb == nk - 1;
-        const int64_t m0 = (t % p.m_tiles) * BM;
-        const int64_t n0 = (t / p.m_tiles) * BN;
+        const Cursor ct = cursor_at(t, 0);  // two divisions per tile, off the per-unit path
+        const int64_t m0 = int64_t(ct.mt) * BM;
+        const int64_t n0 = ct.nt * BN;
         // CTAs whose share starts inside this tile after this one hold the rest of it. A tile owned
         // without its end is always this CTA's last segment: the producer thread stages the
         // contributors' partial tiles (fix-up loader) once all MMAs are done.
@@ -797,7 +822,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync_all();
     const int64_t t = blockIdx.x / C;
     const int r = static_cast<int>(blockIdx.x % C);
-    const int64_t m0 = (t % p.m_tiles) * BM, n0 = (t / p.m_tiles) * BN;
+    const Cursor ct = cursor_at(t, 0);
+    const int64_t m0 = int64_t(ct.mt) * BM, n0 = ct.nt * BN;
     // units: (row, 8-column group) pairs of the rows below M, rows fastest (a warp reads contiguous
     // staged float4s); rank r takes an even share
     const int nrows = static_cast<int>(p.M - m0 < BM ? p.M - m0 : BM);
@@ -880,14 +906,19 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                           const PrefillParams);
 
-template <class DT, int MT>
-KernelFn pick_dt(bool zp, bool two) {
-  if (zp) return two ? prefill_kernel<DT, true, true, MT> : prefill_kernel<DT, true, false, MT>;
-  return two ? prefill_kernel<DT, false, true, MT> : prefill_kernel<DT, false, false, MT>;
+template <class DT, int MT, bool COLS>
+KernelFn pick_zg(bool zp, bool two) {
+  if (zp) return two ? prefill_kernel<DT, true, true, MT, COLS> : prefill_kernel<DT, true, false, MT, COLS>;
+  return two ? prefill_kernel<DT, false, true, MT, COLS> : prefill_kernel<DT, false, false, MT, COLS>;
 }
-KernelFn pick(int dtype, bool zp, bool two, int MT) {
-  if (dtype == W4A16_BF16) return MT == 2 ? pick_dt<BF16, 2>(zp, two) : pick_dt<BF16, 1>(zp, two);
-  return MT == 2 ? pick_dt<F16, 2>(zp, two) : pick_dt<F16, 1>(zp, two);
+template <class DT>
+KernelFn pick_dt(bool zp, bool two, int MT, bool cols) {
+  // one 128-row tile high (MT = 1) never needs the column-fastest order: its row tiles are few
+  if (MT == 1) return pick_zg<DT, 1, false>(zp, two);
+  return cols ? pick_zg<DT, 2, true>(zp, two) : pick_zg<DT, 2, false>(zp, two);
+}
+KernelFn pick(int dtype, bool zp, bool two, int MT, bool cols = false) {
+  return dtype == W4A16_BF16 ? pick_dt<BF16>(zp, two, MT, cols) : pick_dt<F16>(zp, two, MT, cols);
 }
 int smem_of(int MT) { return MT == 2 ? PLayout<2>::kSmemBytes : PLayout<1>::kSmemBytes; }
 
@@ -1068,15 +1099,19 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl, const
     if (!prefill_weight_maps(g, &own)) return cudaErrorInvalidValue;
     wm = &own;
   }
-  const KernelFn fn = pick(g.dtype, zp, two, MT);
+  const int64_t m_tiles = (g.M + BM - 1) / BM, n_tiles = (g.N + BN - 1) / BN;
+  // Consecutive tiles sweep the faster tile dimension; make it the smaller operand's (A: row tiles,
+  // weights: column tiles), so that the larger operand is read from HBM about once.
+  const bool cols = MT == 2 && m_tiles > 1 && g.M * g.K * 2 > g.K * g.N / 2;
+  const KernelFn fn = pick(g.dtype, zp, two, MT, cols);
   {
     static std::mutex mu;
-    static bool configured[64][2][2][2][2] = {};
+    static bool configured[64][2][2][2][2][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
-    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][zp][two][MT - 1];
+    bool &done = configured[dev & 63][g.dtype == W4A16_BF16][zp][two][MT - 1][cols];
     if (!done) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_of(MT));
       if (e != cudaSuccess) return e;
@@ -1084,8 +1119,9 @@ cudaError_t launch_gemm_prefill(const GemmArgs &g, const w4a16_plan_t &pl, const
     }
   }
   PrefillParams prm;
-  prm.m_tiles = static_cast<int>((g.M + BM - 1) / BM);
-  prm.tiles = int64_t(prm.m_tiles) * ((g.N + BN - 1) / BN);
+  prm.m_tiles = static_cast<int>(m_tiles);
+  prm.n_tiles = static_cast<int>(n_tiles);
+  prm.tiles = m_tiles * n_tiles;
   prm.partials = nullptr;
   prm.flags = nullptr;
   if (pl.stream_k) {
